@@ -1,0 +1,194 @@
+"""ctypes binding of libbsc.so: argument marshalling only (every step runs in the CUDA library).
+
+The functions keep the C names of include/bsc.h.  Tensors are torch CUDA tensors; outputs are
+allocated with torch when not given.  A missing library raises at import time: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+BSHD = 0
+SBHD = 1
+
+BSC_OK = 0
+BSC_ERR_DEVICE_TIMEOUT = 6
+
+
+def _load():
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError("libbsc.so is not built (%s); run `python -m block_scaled_causal_gb300.build`" % path)
+    lib = ctypes.CDLL(path)
+    vp, i32, u8p = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+    lib.bsc_abi_version.restype = i32
+    lib.bsc_status_string.restype = ctypes.c_char_p
+    lib.bsc_status_string.argtypes = [i32]
+    for name in ("mxfp8_quantize_qk_rowwise", "mxfp8_quantize_v_colwise", "v_token_normalize"):
+        f = getattr(lib, name)
+        f.restype = i32
+        f.argtypes = [vp, i32, i32, i32, i32, i32, u8p, u8p, vp]
+    lib.mxfp8_quantize_v_fused.restype = i32
+    lib.mxfp8_quantize_v_fused.argtypes = [vp, i32, i32, i32, i32, i32, u8p, u8p, u8p, u8p, vp]
+    lib.mxfp8_causal_attn_fwd.restype = i32
+    lib.mxfp8_causal_attn_fwd.argtypes = [ctypes.POINTER(AttnFwdParams), vp]
+    lib.bsc_read_device_status.restype = i32
+    lib.bsc_read_device_status.argtypes = [vp, vp]
+    return lib
+
+
+class AttnFwdParams(ctypes.Structure):
+    """Mirror of bsc_attn_fwd_params."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("q_sc", ctypes.c_void_p),
+        ("k", ctypes.c_void_p), ("k_sc", ctypes.c_void_p),
+        ("v_t", ctypes.c_void_p), ("v_sc", ctypes.c_void_p),
+        ("vtn", ctypes.c_void_p), ("vtn_sc", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("S", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("D", ctypes.c_int), ("layout", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+        ("p_terms", ctypes.c_int), ("leaky", ctypes.c_int),
+        ("dev_status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32),
+        ("debug_stall", ctypes.c_int),
+    ]
+
+
+lib = _load()
+
+
+class BscError(RuntimeError):
+    def __init__(self, status: int):
+        super().__init__(lib.bsc_status_string(status).decode())
+        self.status = status
+
+
+def _check(status: int):
+    if status != BSC_OK:
+        raise BscError(status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bshd_dims(x: torch.Tensor, layout: int):
+    if x.dim() != 4:
+        raise ValueError("expected a 4-D tensor")
+    if layout == BSHD:
+        B, S, H, D = x.shape
+    else:
+        S, B, H, D = x.shape
+    return B, S, H, D
+
+
+def _require(x: torch.Tensor, dtype, name):
+    if not x.is_cuda or x.dtype != dtype or not x.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+
+
+def mxfp8_quantize_qk_rowwise(x, layout=BSHD, out=None, out_sc=None, stream=None):
+    """Returns (E4M3 bytes shaped like x, row-atom scales [B, H, S/128, 512])."""
+    _require(x, torch.bfloat16, "x")
+    B, S, H, D = _bshd_dims(x, layout)
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if out is None else out
+    out_sc = torch.empty((B, H, max(S // 128, 0), 512), dtype=torch.uint8, device=x.device) \
+        if out_sc is None else out_sc
+    _check(lib.mxfp8_quantize_qk_rowwise(_ptr(x), B, S, H, D, layout, _ptr(out), _ptr(out_sc), _stream(stream)))
+    return out, out_sc
+
+
+def _v_outputs(v, B, S, H, D, col, tn):
+    dev = v.device
+    r = []
+    if col:
+        r += [torch.empty((B, H, D, S), dtype=torch.uint8, device=dev),
+              torch.empty((B, H, max(S // 128, 0), 512), dtype=torch.uint8, device=dev)]
+    if tn:
+        r += [torch.empty(v.shape, dtype=torch.uint8, device=dev),
+              torch.empty((B, H, S), dtype=torch.uint8, device=dev)]
+    return r
+
+
+def mxfp8_quantize_v_colwise(v, layout=BSHD, stream=None):
+    """Returns (E4M3 bytes of V transposed [B, H, D, S], column-atom scales [B, H, S/128, 512])."""
+    _require(v, torch.bfloat16, "v")
+    B, S, H, D = _bshd_dims(v, layout)
+    vt, vsc = _v_outputs(v, B, S, H, D, True, False)
+    _check(lib.mxfp8_quantize_v_colwise(_ptr(v), B, S, H, D, layout, _ptr(vt), _ptr(vsc), _stream(stream)))
+    return vt, vsc
+
+
+def v_token_normalize(v, layout=BSHD, stream=None):
+    """Returns (E4M3 bytes shaped like v, token amplitudes [B, H, S])."""
+    _require(v, torch.bfloat16, "v")
+    B, S, H, D = _bshd_dims(v, layout)
+    vtn, vtn_sc = _v_outputs(v, B, S, H, D, False, True)
+    _check(lib.v_token_normalize(_ptr(v), B, S, H, D, layout, _ptr(vtn), _ptr(vtn_sc), _stream(stream)))
+    return vtn, vtn_sc
+
+
+def mxfp8_quantize_v_fused(v, layout=BSHD, out=None, stream=None):
+    """Both V quantisations in one pass: (v_t, v_sc, vtn, vtn_sc)."""
+    _require(v, torch.bfloat16, "v")
+    B, S, H, D = _bshd_dims(v, layout)
+    vt, vsc, vtn, vtn_sc = _v_outputs(v, B, S, H, D, True, True) if out is None else out
+    _check(lib.mxfp8_quantize_v_fused(_ptr(v), B, S, H, D, layout, _ptr(vt), _ptr(vsc), _ptr(vtn), _ptr(vtn_sc),
+                                      _stream(stream)))
+    return vt, vsc, vtn, vtn_sc
+
+
+def make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, softmax_scale, p_terms=1, leaky=0,
+                     dev_status=None, wait_timeout_ms=0, debug_stall=0):
+    B, S, Hq, D = _bshd_dims(q, layout)
+    Hkv = _bshd_dims(k, layout)[2]
+    return AttnFwdParams(q=q.data_ptr(), q_sc=q_sc.data_ptr(), k=k.data_ptr(), k_sc=k_sc.data_ptr(),
+                         v_t=v_t.data_ptr(), v_sc=v_sc.data_ptr(),
+                         vtn=0 if vtn is None else vtn.data_ptr(), vtn_sc=0 if vtn_sc is None else vtn_sc.data_ptr(),
+                         o=o.data_ptr(), lse=lse.data_ptr(), B=B, S=S, Hq=Hq, Hkv=Hkv, D=D, layout=layout,
+                         softmax_scale=softmax_scale, p_terms=p_terms, leaky=leaky,
+                         dev_status=0 if dev_status is None else dev_status.data_ptr(),
+                         wait_timeout_ms=wait_timeout_ms, debug_stall=debug_stall)
+
+
+def mxfp8_causal_attn_fwd(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, layout=BSHD, softmax_scale=None, p_terms=1,
+                          leaky=0, o=None, lse=None, dev_status=None, wait_timeout_ms=0, debug_stall=0,
+                          stream=None):
+    """Leak-free causal MXFP8 attention forward on quantised operands; returns (O bf16, LSE fp32)."""
+    B, S, Hq, D = _bshd_dims(q, layout)
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if o is None else o
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    p = make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, softmax_scale, p_terms, leaky,
+                         dev_status, wait_timeout_ms, debug_stall)
+    _check(lib.mxfp8_causal_attn_fwd(ctypes.byref(p), _stream(stream)))
+    return o, lse
+
+
+def bsc_read_device_status(dev_status, stream=None):
+    """Synchronises the stream; returns the library status for the device status word."""
+    return lib.bsc_read_device_status(_ptr(dev_status), _stream(stream))
+
+
+def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, stream=None):
+    """The whole hot path on bf16 inputs: quantise Q, K rowwise, V columnwise + token-normalised,
+    then the leak-free causal attention forward.  Returns (O bf16, LSE fp32)."""
+    qq, qs = mxfp8_quantize_qk_rowwise(q, layout, stream=stream)
+    kq, ks = mxfp8_quantize_qk_rowwise(k, layout, stream=stream)
+    if leaky:
+        vt, vsc = mxfp8_quantize_v_colwise(v, layout, stream=stream)
+        vtn = vtn_sc = None
+    else:
+        vt, vsc, vtn, vtn_sc = mxfp8_quantize_v_fused(v, layout, stream=stream)
+    return mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, p_terms, leaky,
+                                 stream=stream)

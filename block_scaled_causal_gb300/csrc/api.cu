@@ -1,0 +1,213 @@
+// C-ABI entry points: argument checks, tensor-map creation, launches.  See include/bsc.h.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/bsc.h"
+#include "bsc_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device capability check, cached per device ordinal.
+bsc_status check_device() {
+  static std::mutex mu;
+  static int cached[64];   // 0 unknown, 1 ok, 2 bad
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSC_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return BSC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return BSC_ERR_CUDA;
+    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return cached[dev] == 1 ? BSC_OK : BSC_ERR_UNSUPPORTED;
+}
+
+// Common shape checks.  Returns BSC_OK with *empty set when there is nothing to do.
+bsc_status check_shape(int B, int S, int H, int D, int layout, bool* empty) {
+  *empty = false;
+  if (B < 0 || S < 0 || H < 0 || D < 0) return BSC_ERR_SHAPE;
+  if (layout != BSC_BSHD && layout != BSC_SBHD) return BSC_ERR_SHAPE;
+  if (B == 0 || S == 0 || H == 0) {
+    *empty = true;
+    return BSC_OK;
+  }
+  if (D != 128 || S % 128 != 0) return BSC_ERR_UNSUPPORTED;
+  // every index the kernels form fits in 64 bits; the grids must fit their limits
+  if ((long long)B * H * (S / 128) >= (1LL << 31)) return BSC_ERR_UNSUPPORTED;
+  return BSC_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// E4M3 [.., S, .., H, 128] operand as a 4-D map {D, H, S, B} with a 128-token x 128-byte box.
+bool encode_tokens_map(CUtensorMap* m, const void* base, int B, int S, int H, int layout, bool swizzle) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  const cuuint64_t sH = 128;
+  const cuuint64_t sS = layout == BSC_BSHD ? (cuuint64_t)H * 128 : (cuuint64_t)B * H * 128;
+  const cuuint64_t sB = layout == BSC_BSHD ? (cuuint64_t)S * H * 128 : (cuuint64_t)H * 128;
+  const cuuint64_t strides[3] = {sH, sS, sB};
+  const cuuint32_t box[4] = {128, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Transposed V bytes [rows = B*H*D][S] as a 2-D map with a 128-key x 128-row box.
+bool encode_vt_map(CUtensorMap* m, const void* base, long long rows, int S) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)S, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)S};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bsc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BSC_OK : BSC_ERR_CUDA; }
+
+bsc_status quant_v_common(const void* v, int B, int S, int H, int D, bsc_layout layout, uint8_t* vt, uint8_t* vsc,
+                          uint8_t* vtn, uint8_t* vtn_sc, bsc_stream_t stream, bool want_col, bool want_tn) {
+  bool empty;
+  bsc_status s = check_shape(B, S, H, D, layout, &empty);
+  if (s != BSC_OK || empty) return s;
+  if (!v || (want_col && (!vt || !vsc)) || (want_tn && (!vtn || !vtn_sc))) return BSC_ERR_NULL;
+  if (!aligned16(v) || (want_col && (!aligned16(vt) || !aligned16(vsc))) ||
+      (want_tn && (!aligned16(vtn) || !aligned16(vtn_sc))))
+    return BSC_ERR_ALIGN;
+  if ((s = check_device()) != BSC_OK) return s;
+  return from_cuda(bsc::launch_quant_v(v, want_col ? vt : nullptr, want_col ? vsc : nullptr,
+                                       want_tn ? vtn : nullptr, want_tn ? vtn_sc : nullptr, B, S, H, layout,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int bsc_abi_version(void) { return 1; }
+
+const char* bsc_status_string(bsc_status s) {
+  switch (s) {
+    case BSC_OK: return "BSC_OK";
+    case BSC_ERR_NULL: return "BSC_ERR_NULL: a required pointer is NULL";
+    case BSC_ERR_SHAPE: return "BSC_ERR_SHAPE: invalid sizes, head grouping or layout";
+    case BSC_ERR_ALIGN: return "BSC_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case BSC_ERR_UNSUPPORTED: return "BSC_ERR_UNSUPPORTED: unsupported size, option or device";
+    case BSC_ERR_CUDA: return "BSC_ERR_CUDA: a CUDA call failed";
+    case BSC_ERR_DEVICE_TIMEOUT: return "BSC_ERR_DEVICE_TIMEOUT: a device-side wait gave up";
+  }
+  return "unknown bsc_status";
+}
+
+bsc_status mxfp8_quantize_qk_rowwise(const void* x, int B, int S, int H, int D, bsc_layout layout, uint8_t* xq,
+                                     uint8_t* xsc, bsc_stream_t stream) {
+  bool empty;
+  bsc_status s = check_shape(B, S, H, D, layout, &empty);
+  if (s != BSC_OK || empty) return s;
+  if (!x || !xq || !xsc) return BSC_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xq) || !aligned16(xsc)) return BSC_ERR_ALIGN;
+  if ((s = check_device()) != BSC_OK) return s;
+  return from_cuda(bsc::launch_quant_rowwise(x, xq, xsc, B, S, H, layout, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bsc_status mxfp8_quantize_v_colwise(const void* v, int B, int S, int H, int D, bsc_layout layout, uint8_t* vt,
+                                    uint8_t* vsc, bsc_stream_t stream) {
+  return quant_v_common(v, B, S, H, D, layout, vt, vsc, nullptr, nullptr, stream, true, false);
+}
+
+bsc_status v_token_normalize(const void* v, int B, int S, int H, int D, bsc_layout layout, uint8_t* vtn,
+                             uint8_t* vtn_sc, bsc_stream_t stream) {
+  return quant_v_common(v, B, S, H, D, layout, nullptr, nullptr, vtn, vtn_sc, stream, false, true);
+}
+
+bsc_status mxfp8_quantize_v_fused(const void* v, int B, int S, int H, int D, bsc_layout layout, uint8_t* vt,
+                                  uint8_t* vsc, uint8_t* vtn, uint8_t* vtn_sc, bsc_stream_t stream) {
+  return quant_v_common(v, B, S, H, D, layout, vt, vsc, vtn, vtn_sc, stream, true, true);
+}
+
+bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stream) {
+  if (!p) return BSC_ERR_NULL;
+  if (p->Hq < 0 || p->Hkv < 0) return BSC_ERR_SHAPE;
+  bool empty;
+  bsc_status s = check_shape(p->B, p->S, p->Hq, p->D, p->layout, &empty);
+  if (s != BSC_OK) return s;
+  if (!empty && p->Hkv == 0) return BSC_ERR_SHAPE;
+  if (empty) return BSC_OK;
+  if (p->Hq % p->Hkv != 0) return BSC_ERR_SHAPE;
+  if (p->p_terms != 1 && p->p_terms != 2) return BSC_ERR_UNSUPPORTED;
+  if (p->leaky != 0 && p->leaky != 1) return BSC_ERR_UNSUPPORTED;
+  const bool own = p->leaky == 0;
+  if (!p->q || !p->q_sc || !p->k || !p->k_sc || !p->v_t || !p->v_sc || !p->o || !p->lse) return BSC_ERR_NULL;
+  if (own && (!p->vtn || !p->vtn_sc)) return BSC_ERR_NULL;
+  const void* ptrs[] = {p->q, p->q_sc, p->k, p->k_sc, p->v_t, p->v_sc, p->o, p->lse, p->dev_status};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return BSC_ERR_ALIGN;
+  if (own && (!aligned16(p->vtn) || !aligned16(p->vtn_sc))) return BSC_ERR_ALIGN;
+  if ((s = check_device()) != BSC_OK) return s;
+
+  bsc::AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_tokens_map(&a.tm_q, p->q, p->B, p->S, p->Hq, p->layout, true) ||
+      !encode_tokens_map(&a.tm_k, p->k, p->B, p->S, p->Hkv, p->layout, true) ||
+      !encode_vt_map(&a.tm_v, p->v_t, (long long)p->B * p->Hkv * 128, p->S))
+    return BSC_ERR_CUDA;
+  if (own && !encode_tokens_map(&a.tm_vtn, p->vtn, p->B, p->S, p->Hkv, p->layout, false)) return BSC_ERR_CUDA;
+  a.q_sc = p->q_sc;
+  a.k_sc = p->k_sc;
+  a.v_sc = p->v_sc;
+  a.vtn_sc = own ? p->vtn_sc : nullptr;
+  a.o = p->o;
+  a.lse = p->lse;
+  a.dev_status = p->dev_status;
+  a.limit_ns = (unsigned long long)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
+  a.B = p->B;
+  a.S = p->S;
+  a.Hq = p->Hq;
+  a.Hkv = p->Hkv;
+  a.layout = p->layout;
+  a.scale_log2e = (float)((double)p->softmax_scale * 1.4426950408889634);
+  a.p_terms = p->p_terms;
+  a.leaky = p->leaky;
+  a.inject_stall = p->debug_stall ? 1 : 0;
+  return from_cuda(bsc::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bsc_status bsc_read_device_status(const int32_t* dev_status, bsc_stream_t stream) {
+  if (!dev_status) return BSC_ERR_NULL;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, reinterpret_cast<cudaStream_t>(stream)) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSC_ERR_CUDA;
+  return v == 0 ? BSC_OK : BSC_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

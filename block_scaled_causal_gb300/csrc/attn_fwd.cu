@@ -1,0 +1,451 @@
+// Leak-free causal MXFP8 attention forward for sm_103a (tcgen05 / TMEM / TMA).
+//
+// "[PyTorch] Add causal MXFP8 attention without future-token leakage through V scales"
+// (TransformerEngine PR #3865), Description:
+//   * keys in completed 32-token blocks (j < 32*floor(i/32)) are attended in MXFP8 with V quantised
+//     columnwise (one scale per 32 consecutive tokens), so every V scale read covers visible tokens;
+//   * the query's own block (at most 32 keys, j <= i) is attended on the token-normalised V copy;
+//   * the two partials are merged through their log-sum-exps.
+// Here both key sets share one running softmax (max m and sum l) per row, which is the same merge
+// done incrementally, and both P.V products accumulate into one fp32 O accumulator in TMEM.
+//
+// One CTA computes one 128-row query tile t of one (batch, query head) and walks key tiles 0..t.
+// Warp roles (256 threads):
+//   warp 0     TMA producer: Q tile + scales once; K, V (columnwise, transposed) tiles + scales
+//              through a 2-stage ring; the own-block token-normalised V tile once.
+//   warp 1     allocates TMEM; lane 0 issues tcgen05.cp (scale factors) and tcgen05.mma.
+//   warps 2-3  decode the token-normalised V tile to BF16 (exact) in the MMA operand layout.
+//   warps 4-7  softmax, one query row per thread (TMEM lane = row), then the epilogue.
+// TMEM (512 columns): S[0] 0-127, S[1] 128-255, O 256-383, scale factors from 384.
+// P (E4M3, 32 columns per term) is written over the S buffer it came from; the own-block BF16 P
+// goes to the other S buffer.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "bsc_internal.h"
+#include "ptx.cuh"
+
+namespace bsc {
+
+namespace {
+
+constexpr int BM = 128;   // query rows per tile
+constexpr int BN = 128;   // keys per tile
+constexpr int HD = 128;   // head dimension
+constexpr int kThreads = 256;
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + BM * HD;             // 2 stages
+constexpr uint32_t OFF_V = OFF_K + 2 * BN * HD;         // 2 stages (d rows x 128 keys)
+constexpr uint32_t OFF_VT = OFF_V + 2 * HD * BN;        // own-block V, BF16, 2 K-atoms of 16 KB
+constexpr uint32_t OFF_VTN8 = OFF_VT + 2 * HD * BN;     // raw token-normalised bytes [key][d]
+constexpr uint32_t OFF_SFQ = OFF_VTN8 + BN * HD;
+constexpr uint32_t OFF_SFK = OFF_SFQ + 512;             // 2 stages
+constexpr uint32_t OFF_SFV = OFF_SFK + 2 * 512;         // 2 stages
+constexpr uint32_t OFF_SFP = OFF_SFV + 2 * 512;         // P scale blocks: term 0, term 1
+constexpr uint32_t OFF_VTNSC = OFF_SFP + 2 * 512;       // 128 token amplitudes
+constexpr uint32_t OFF_BAR = OFF_VTNSC + 128;
+constexpr uint32_t NUM_BARS = 20;
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem slot, abort flag
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // alignment slack
+
+enum Bar : uint32_t {
+  B_Q_FULL = 0,
+  B_K_FULL = 1,    // +stage
+  B_K_EMPTY = 3,   // +stage
+  B_V_FULL = 5,    // +stage
+  B_V_EMPTY = 7,   // +stage
+  B_S_FULL = 9,    // +buffer
+  B_P_FULL = 11,   // +buffer
+  B_PV_DONE = 13,
+  B_O_FULL = 14,
+  B_VTN_FULL = 15,
+  B_VT_READY = 16,
+  B_DRAIN = 17,
+  B_INJECT = 18,
+};
+
+// TMEM column map
+constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_SFQ = 384, T_SFK = 388, T_SFV = 396, T_SFP = 404;
+
+// P scale bytes: term 0 holds P * 2^8, term 1 the residual * 2^12.
+constexpr uint8_t SFP_TERM0 = 127 - 8;
+constexpr uint8_t SFP_TERM1 = 127 - 12;
+
+// wait-site codes reported through the device status word
+enum Site : int {
+  W_PROD_KEMPTY = 1, W_PROD_VEMPTY, W_MMA_Q, W_MMA_K, W_MMA_V, W_MMA_P, W_MMA_VT, W_MMA_INJECT,
+  W_SM_S, W_SM_PV, W_SM_O, W_DEC_VTN,
+};
+
+__device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
+  return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);   // 2^(sb-127), sb <= 254
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](uint32_t i) { return sbase + OFF_BAR + 8u * i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.S / BM;
+  // heaviest tiles first; the query heads sharing a KV head are adjacent
+  const int bh = blockIdx.x % (a.B * a.Hq);
+  const int t = T - 1 - (int)(blockIdx.x / (a.B * a.Hq));
+  const int hq = bh % a.Hq, b = bh / a.Hq;
+  const int hk = hq / (a.Hq / a.Hkv);
+  const bool own_split = !a.leaky;
+
+  // ---- setup
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_Q_FULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_K_FULL + s), 1);
+      mbar_init(bar(B_K_EMPTY + s), 1);
+      mbar_init(bar(B_V_FULL + s), 1);
+      mbar_init(bar(B_V_EMPTY + s), 1);
+      mbar_init(bar(B_S_FULL + s), 1);
+      mbar_init(bar(B_P_FULL + s), 128);
+    }
+    mbar_init(bar(B_PV_DONE), 1);
+    mbar_init(bar(B_O_FULL), 1);
+    mbar_init(bar(B_VTN_FULL), 1);
+    mbar_init(bar(B_VT_READY), 64);
+    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_INJECT), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + OFF_MISC, 512);
+    tmem_relinquish();
+  }
+  // constant P scale blocks
+  for (int i = threadIdx.x; i < 256; i += kThreads) {
+    reinterpret_cast<uint32_t*>(smem + OFF_SFP)[i] = i < 128 ? SFP_TERM0 * 0x01010101u : SFP_TERM1 * 0x01010101u;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, a.dev_status, a.limit_ns};
+
+  if (warp == 0) {
+    // ======================= producer
+    if (lane == 0) {
+      prefetch_tensormap(&a.tm_q);
+      prefetch_tensormap(&a.tm_k);
+      prefetch_tensormap(&a.tm_v);
+      const long long kv_plane = (long long)b * a.Hkv + hk;
+      mbar_arrive_expect_tx(bar(B_Q_FULL), BM * HD + 512);
+      tma_load_4d(sbase + OFF_Q, &a.tm_q, bar(B_Q_FULL), 0, hq, t * BM, b);
+      bulk_load(sbase + OFF_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + t) * 512, 512, bar(B_Q_FULL));
+      int nk[2] = {0, 0}, nv[2] = {0, 0};   // loads issued per stage
+      bool ok = true;
+      for (int j = 0; j <= t && ok; ++j) {
+        const int st = j & 1, n = j >> 1;
+        if (n > 0 && !(ok = mbar_wait(bar(B_K_EMPTY + st), (n - 1) & 1, ctl, W_PROD_KEMPTY))) break;
+        mbar_arrive_expect_tx(bar(B_K_FULL + st), BN * HD + 512);
+        tma_load_4d(sbase + OFF_K + st * BN * HD, &a.tm_k, bar(B_K_FULL + st), 0, hk, j * BN, b);
+        bulk_load(sbase + OFF_SFK + st * 512, a.k_sc + (kv_plane * T + j) * 512, 512, bar(B_K_FULL + st));
+        ++nk[st];
+        if (n > 0 && !(ok = mbar_wait(bar(B_V_EMPTY + st), (n - 1) & 1, ctl, W_PROD_VEMPTY))) break;
+        mbar_arrive_expect_tx(bar(B_V_FULL + st), HD * BN + 512);
+        tma_load_2d(sbase + OFF_V + st * HD * BN, &a.tm_v, bar(B_V_FULL + st), j * BN, (int)(kv_plane * HD));
+        bulk_load(sbase + OFF_SFV + st * 512, a.v_sc + (kv_plane * T + j) * 512, 512, bar(B_V_FULL + st));
+        ++nv[st];
+      }
+      bool vtn_issued = false;
+      if (own_split && ok) {
+        prefetch_tensormap(&a.tm_vtn);
+        mbar_arrive_expect_tx(bar(B_VTN_FULL), BN * HD + BN);
+        tma_load_4d(sbase + OFF_VTN8, &a.tm_vtn, bar(B_VTN_FULL), 0, hk, t * BN, b);
+        bulk_load(sbase + OFF_VTNSC, a.vtn_sc + kv_plane * a.S + (long long)t * BN, BN, bar(B_VTN_FULL));
+        vtn_issued = true;
+      }
+      // drain: every copy this thread issued must land before the CTA may exit
+      for (int st = 0; st < 2; ++st) {
+        if (nk[st] > 0) mbar_wait_drain(bar(B_K_FULL + st), (nk[st] - 1) & 1, a.limit_ns);
+        if (nv[st] > 0) mbar_wait_drain(bar(B_V_FULL + st), (nv[st] - 1) & 1, a.limit_ns);
+      }
+      mbar_wait_drain(bar(B_Q_FULL), 0, a.limit_ns);
+      if (vtn_issued) mbar_wait_drain(bar(B_VTN_FULL), 0, a.limit_ns);
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer
+    if (lane == 0) {
+      const uint32_t tS[2] = {tmem + T_S0, tmem + T_S1};
+      const uint32_t tO = tmem + T_O;
+      bool ok = true;
+      if (a.inject_stall) ok = mbar_wait(bar(B_INJECT), 0, ctl, W_MMA_INJECT);   // nothing arrives here
+      ok = ok && mbar_wait(bar(B_Q_FULL), 0, ctl, W_MMA_Q);
+      if (ok) {
+        tc_fence_after();
+        tc_cp_32x128b_warpx4(tmem + T_SFQ, desc_sf_block(sbase + OFF_SFQ));
+        tc_cp_32x128b_warpx4(tmem + T_SFP, desc_sf_block(sbase + OFF_SFP));
+        tc_cp_32x128b_warpx4(tmem + T_SFP + 4, desc_sf_block(sbase + OFF_SFP + 512));
+      }
+      auto pv = [&](int jj) -> bool {
+        const int st = jj & 1, n = jj >> 1;
+        if (!mbar_wait(bar(B_V_FULL + st), n & 1, ctl, W_MMA_V)) return false;
+        if (!mbar_wait(bar(B_P_FULL + st), n & 1, ctl, W_MMA_P)) return false;
+        tc_fence_after();
+        tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * st, desc_sf_block(sbase + OFF_SFV + st * 512));
+        for (int term = 0; term < a.p_terms; ++term) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8_ts(tO, tS[st] + term * 32 + kk * 8,
+                        desc_kmajor_sw128(sbase + OFF_V + st * HD * BN + kk * 32), idesc_mxf8(BM, HD, kk, kk),
+                        tmem + T_SFP + 4 * term, tmem + T_SFV + 4 * st, (jj > 0 || term > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        if (jj == t && own_split) {
+          if (!mbar_wait(bar(B_VT_READY), 0, ctl, W_MMA_VT)) return false;
+          tc_fence_after();
+          for (int term = 0; term < a.p_terms; ++term) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+              mma_f16_ts(tO, tS[st ^ 1] + term * 64 + s * 8,
+                         desc_kmajor_sw128(sbase + OFF_VT + (s >> 2) * (HD * 128) + (s & 3) * 32),
+                         idesc_bf16(BM, HD), 1u);
+            }
+          }
+        }
+        tc_commit(bar(B_V_EMPTY + st));
+        tc_commit(bar(B_PV_DONE));
+        return true;
+      };
+      for (int j = 0; j <= t && ok; ++j) {
+        const int st = j & 1, n = j >> 1;
+        if (!(ok = mbar_wait(bar(B_K_FULL + st), n & 1, ctl, W_MMA_K))) break;
+        tc_fence_after();
+        tc_cp_32x128b_warpx4(tmem + T_SFK + 4 * st, desc_sf_block(sbase + OFF_SFK + st * 512));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          mma_mxf8_ss(tS[st], desc_kmajor_sw128(sbase + OFF_Q + kk * 32),
+                      desc_kmajor_sw128(sbase + OFF_K + st * BN * HD + kk * 32), idesc_mxf8(BM, BN, kk, kk),
+                      tmem + T_SFQ, tmem + T_SFK + 4 * st, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(B_S_FULL + st));
+        tc_commit(bar(B_K_EMPTY + st));
+        if (j >= 1) ok = pv(j - 1);
+      }
+      if (ok) ok = pv(t);
+      if (ok) tc_commit(bar(B_O_FULL));
+      // drain every tcgen05 operation this thread issued before TMEM is released
+      tc_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, a.limit_ns);
+    }
+  } else if (warp < 4) {
+    // ======================= own-block V decode (64 threads)
+    if (own_split) {
+      const int u = threadIdx.x - 64;
+      if (__all_sync(0xFFFFFFFFu, mbar_wait(bar(B_VTN_FULL), 0, ctl, W_DEC_VTN))) {
+        const uint8_t* raw = smem + OFF_VTN8;
+        const uint8_t* amp = smem + OFF_VTNSC;
+        for (int half = 0; half < 2; ++half) {
+          const int d = u + 64 * half;
+          for (int kc = 0; kc < 16; ++kc) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k0 = kc * 8 + 2 * e;
+              const uint16_t pair = (uint16_t)raw[k0 * HD + d] | ((uint16_t)raw[(k0 + 1) * HD + d] << 8);
+              const uint32_t h2 = cvt_e4m3x2_to_f16x2(pair);
+              const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * pow2_e8m0(amp[k0]);
+              const float v1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * pow2_e8m0(amp[k0 + 1]);
+              w[e] = pack_bf16x2(v0, v1);
+            }
+            const uint32_t off = OFF_VT + (kc >> 3) * (HD * 128) + d * 128 + (((kc & 7) ^ (d & 7)) * 16);
+            *reinterpret_cast<uint4*>(smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(bar(B_VT_READY));
+    }
+  } else {
+    // ======================= softmax + epilogue (128 threads, one row each)
+    const int q = warp - 4;             // TMEM lane quarter == 32-row query sub-block of the tile
+    const int r = q * 32 + lane;        // row inside the tile
+    const int i = t * BM + r;           // query token
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const float sl2 = a.scale_log2e;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j <= t; ++j) {
+      const int st = j & 1, n = j >> 1;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + st), n & 1, ctl, W_SM_S));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tSb = tmem + (st ? T_S1 : T_S0) + lane_off;
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tSb + 32 * c, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[32 * c + k] = __uint_as_float(rr[k]) * sl2;
+      }
+      const bool diag = (j == t);
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = (c > r) ? -INFINITY : x[c];
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int c = 1; c < 127; c += 2) mt = fmax3(mt, x[c], x[c + 1]);
+      mt = fmaxf(mt, x[127]);
+      const float m_new = fmaxf(m, mt);
+      const bool grow = (j > 0) && (m_new > m);
+      bool pv_waited = false;
+      if (__any_sync(0xFFFFFFFFu, grow)) {
+        // rescale this warp's O rows (factor 1 for rows whose max did not move): needs PV_{j-1} done
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_PV_DONE), (j - 1) & 1, ctl, W_SM_PV));
+        if (!ok) break;
+        pv_waited = true;
+        tc_fence_after();
+        const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+        const uint32_t tOb = tmem + T_O + lane_off;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tOb + 32 * c, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) rr[k] = __float_as_uint(__uint_as_float(rr[k]) * alpha);
+          tmem_st32(tOb + 32 * c, rr);
+        }
+      }
+      const float alpha_l = grow ? ex2_approx(m - m_new) : 1.0f;
+      // p' = 2^(x - m_new + 8) = 256 * p
+      const float mb = m_new - 8.0f;
+      float rowsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        x[c] = ex2_approx(x[c] - mb);
+        rowsum += x[c];
+      }
+      l = l * alpha_l + rowsum;
+      m = m_new;
+      // E4M3 P for completed keys; in the diagonal tile keys of the own and later 32-blocks are 0
+      // (the leaky control keeps the own block here instead).
+      const int fp8_limit = diag ? (a.leaky ? q + 1 : q) : 4;   // 32-key blocks kb < limit use this path
+      uint32_t w0[32], w1[32];
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const bool use = kb < fp8_limit;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const int c = kb * 32 + g * 4;
+          const float p0 = use ? x[c] : 0.f, p1 = use ? x[c + 1] : 0.f;
+          const float p2 = use ? x[c + 2] : 0.f, p3 = use ? x[c + 3] : 0.f;
+          const uint16_t h01 = cvt_e4m3x2(p0, p1), h23 = cvt_e4m3x2(p2, p3);
+          w0[kb * 8 + g] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+          if (a.p_terms > 1) {
+            const uint32_t f01 = cvt_e4m3x2_to_f16x2(h01), f23 = cvt_e4m3x2_to_f16x2(h23);
+            const float d0 = p0 - __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFFu)));
+            const float d1 = p1 - __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
+            const float d2 = p2 - __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFFu)));
+            const float d3 = p3 - __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
+            w1[kb * 8 + g] = (uint32_t)cvt_e4m3x2(d0 * 16.f, d1 * 16.f) |
+                             ((uint32_t)cvt_e4m3x2(d2 * 16.f, d3 * 16.f) << 16);
+          }
+        }
+      }
+      tmem_st32(tSb, w0);
+      if (a.p_terms > 1) tmem_st32(tSb + 32, w1);
+      if (diag && own_split) {
+        // own block (keys of sub-block q, j <= i) as BF16 P (1 or 2 terms) into the other S buffer,
+        // which PV_{t-1} may still be reading
+        if (t > 0 && !pv_waited) {
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_PV_DONE), (t - 1) & 1, ctl, W_SM_PV));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t tPo = tmem + (st ? T_S0 : T_S1) + lane_off;
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = kb * 32 + 2 * e;
+            const float p0 = (kb == q) ? x[c] * (1.0f / 256.0f) : 0.f;
+            const float p1 = (kb == q) ? x[c + 1] * (1.0f / 256.0f) : 0.f;
+            const uint32_t h = pack_bf16x2(p0, p1);
+            const float r0 = p0 - __uint_as_float(h << 16), r1 = p1 - __uint_as_float(h & 0xFFFF0000u);
+            const int idx = (kb & 1) * 16 + e;
+            hi[idx] = h;
+            lo[idx] = pack_bf16x2(r0, r1);
+          }
+          if (kb & 1) {
+            tmem_st32(tPo + (kb >> 1) * 32, hi);
+            if (a.p_terms > 1) tmem_st32(tPo + 64 + (kb >> 1) * 32, lo);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_FULL + st));
+    }
+    // ---- epilogue: O / l -> BF16, LSE (natural log)
+    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_O_FULL), 0, ctl, W_SM_O));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 256.0f / l;
+      const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq
+                                          : ((long long)i * a.B + b) * a.Hq + hq;
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + row * HD);
+      const uint32_t tOb = tmem + T_O + lane_off;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tOb + 32 * c, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = g * 8 + 2 * e;
+            w[e] = pack_bf16x2(__uint_as_float(rr[k]) * inv_l, __uint_as_float(rr[k + 1]) * inv_l);
+          }
+          orow[c * 4 + g] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      const float ln2 = 0.69314718055994531f;
+      a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m + lg2_approx(l) - 8.0f) * ln2;
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnArgs& args, cudaStream_t st) {
+  static bool attr_set = false;   // per-process; the attribute is per function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long ctas = (long long)args.B * args.Hq * (args.S / BM);
+  attn_fwd_kernel<<<(unsigned)ctas, kThreads, SMEM_BYTES, st>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace bsc

@@ -1,0 +1,37 @@
+// Internal launch interface shared by the C-ABI layer and the kernels (not part of the ABI).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsc {
+
+cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, int S, int H, int layout,
+                                 cudaStream_t st);
+cudaError_t launch_quant_v(const void* v, uint8_t* vt, uint8_t* vsc, uint8_t* vtn, uint8_t* vtn_sc, int B, int S,
+                           int H, int layout, cudaStream_t st);
+
+// Everything the attention kernel reads, by value (tensor maps must be 64-byte aligned).
+struct AttnArgs {
+  CUtensorMap tm_q;     // Q bytes, 4-D {D, Hq, S, B}, box {128,1,128,1}, 128-byte swizzle
+  CUtensorMap tm_k;     // K bytes, 4-D {D, Hkv, S, B}, same box
+  CUtensorMap tm_v;     // V columnwise bytes, 2-D {S, B*Hkv*D}, box {128,128}, 128-byte swizzle
+  CUtensorMap tm_vtn;   // token-normalised V bytes, 4-D like K, no swizzle
+  const uint8_t* q_sc;
+  const uint8_t* k_sc;
+  const uint8_t* v_sc;
+  const uint8_t* vtn_sc;
+  void* o;
+  float* lse;
+  int32_t* dev_status;
+  unsigned long long limit_ns;
+  int B, S, Hq, Hkv, layout;
+  float scale_log2e;
+  int p_terms;
+  int leaky;
+  int inject_stall;
+};
+
+cudaError_t launch_attn_fwd(const AttnArgs& args, cudaStream_t st);
+
+}  // namespace bsc

@@ -1,0 +1,187 @@
+// MXFP8 quantisers for the attention operands (HBM-bound streaming kernels).
+//
+// "[PyTorch] Add causal MXFP8 attention without future-token leakage through V scales"
+// (TransformerEngine PR #3865), Description:
+//   * Q and K are quantised rowwise: E4M3 bytes with one E8M0 scale per 32 elements along D;
+//   * V is quantised columnwise: one shared scale per 32 consecutive tokens;
+//   * the token-normalised copy of V carries one power-of-two amplitude per token.
+// Scale rule (OCP MX, E4M3 elements): scale byte = floor(log2 amax) - 8 + 127, clamped to [0, 254];
+// elements x * 2^-e rounded to nearest even on the E4M3 grid, saturating at 448; a block holding a
+// NaN or an infinity gets scale 0xFF and element bytes 0x7F.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "bsc_internal.h"
+
+namespace bsc {
+
+// |x| as bf16 bit patterns for 8 packed values; the unsigned maximum of these patterns orders
+// finite magnitudes correctly and puts Inf/NaN above every finite value.
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4& v) {
+  uint32_t a = v.x & 0x7FFF7FFFu, b = v.y & 0x7FFF7FFFu, c = v.z & 0x7FFF7FFFu, d = v.w & 0x7FFF7FFFu;
+  uint32_t m;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+  asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(c));
+  asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(d));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 8 bf16 values (one uint4) * inv_scale -> 8 E4M3 bytes (one uint2).
+__device__ __forceinline__ uint2 quant8(const uint4& v, float inv, bool nonfinite) {
+  if (nonfinite) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint16_t p0 = cvt_e4m3x2(bf16_lo(w[2 * i]) * inv, bf16_hi(w[2 * i]) * inv);
+    const uint16_t p1 = cvt_e4m3x2(bf16_lo(w[2 * i + 1]) * inv, bf16_hi(w[2 * i + 1]) * inv);
+    out[i] = (uint32_t)p0 | ((uint32_t)p1 << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+// Byte offset of row m's 32-bit scale word inside a 128-row scale atom (F8_128x4 order):
+// rows m and m + 32 sit in adjacent words of the same 16-byte line.
+__device__ __forceinline__ uint32_t atom_word_offset(uint32_t m) { return (m & 31u) * 16u + ((m >> 5) & 3u) * 4u; }
+
+// ------------------------------------------------------------------------------------------
+// Rowwise quantiser (Q, K): one thread per 16 bytes (8 elements); 16 threads per 128-element row;
+// a 32-element block is 4 adjacent threads.  Rows are visited in memory order; (b, s, h) of a row
+// follows from the layout.  Scale words go to the atom layout
+//   sc[((b*H + h) * (S/128) + s/128) * 512 + (s%32)*16 + ((s%128)/32)*4 + c],  c = d / 32.
+__global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint4* __restrict__ x, uint2* __restrict__ q,
+                                                            uint8_t* __restrict__ sc, long long nrows, int B,
+                                                            int S, int H, int layout) {
+  const long long chunk = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = chunk >> 4;
+  const bool active = row < nrows;
+  const uint4 v = active ? __ldcs(&x[chunk]) : make_uint4(0, 0, 0, 0);
+  uint32_t am = absmax_bits8(v);
+  am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+  am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+  float inv;
+  const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv);
+  if (active) __stcs(&q[chunk], quant8(v, inv, sb == 0xFFu));
+  // gather the 4 block scales of this row on its first thread
+  const int lane = threadIdx.x & 31;
+  const int base = lane & 16;
+  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, base + 4);
+  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 8);
+  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 12);
+  if (active && (lane & 15) == 0) {
+    long long b, s, h;
+    h = row % H;
+    const long long r2 = row / H;
+    if (layout == 0) { s = r2 % S; b = r2 / S; }
+    else { b = r2 % B; s = r2 / B; }
+    const long long plane = b * H + h;
+    const long long off = (plane * (S / 128) + s / 128) * 512 + atom_word_offset((uint32_t)(s & 127));
+    *reinterpret_cast<uint32_t*>(sc + off) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// V quantiser: one CTA per (b, h, 128-token tile), 256 threads.  Produces either or both of
+//   * the columnwise copy, transposed: vt[((b*H + h)*D + d)*S + s], with scale atoms
+//       vsc[((b*H + h)*(S/128) + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32];
+//   * the token-normalised copy in V's own layout with scales vtn_sc[(b*H + h)*S + s].
+constexpr int VQ_ROWS = 128;
+constexpr int VQ_PITCH = 256 + 16;   // bytes per staged token row
+
+__global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+                                                      uint8_t* __restrict__ vsc, uint8_t* __restrict__ vtn,
+                                                      uint8_t* __restrict__ vtn_sc, int B, int S, int H,
+                                                      int layout) {
+  __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
+  const int ntiles = S / VQ_ROWS;
+  const int tile_idx = blockIdx.x % ntiles;
+  const int plane = blockIdx.x / ntiles;   // b*H + h
+  const int h = plane % H, b = plane / H;
+  const int s0 = tile_idx * VQ_ROWS;
+  const int tid = threadIdx.x;
+  const long long row_stride = layout == 0 ? (long long)H * 128 : (long long)B * H * 128;   // elements per s
+  const long long base0 = layout == 0 ? (((long long)b * S) * H + h) * 128 : ((long long)b * H + h) * 128;
+
+  // load: 16 threads per token row, 8 rows per pass of 128 threads... 2048 chunks / 256 threads
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int c = it * 256 + tid;
+    const int r = c >> 4, l16 = c & 15;
+    const long long e = base0 + (long long)(s0 + r) * row_stride + l16 * 8;
+    const uint4 val = __ldcs(reinterpret_cast<const uint4*>(v + e * 2));
+    *reinterpret_cast<uint4*>(&tile[r * VQ_PITCH + l16 * 16]) = val;
+    if (vtn != nullptr) {
+      // token-normalised copy straight from registers: the 16 threads of a row reduce its amax
+      uint32_t am = absmax_bits8(val);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+      float inv;
+      const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv);
+      __stcs(reinterpret_cast<uint2*>(vtn + e), quant8(val, inv, sb == 0xFFu));
+      if (l16 == 0) vtn_sc[(long long)plane * S + s0 + r] = (uint8_t)sb;
+    }
+  }
+  if (vt == nullptr) return;
+  __syncthreads();
+
+  // columnwise: thread -> (pair of d columns, 32-token block)
+  const int dp = tid & 63;      // d = 2*dp, 2*dp + 1
+  const int kb = tid >> 6;      // 32-token block inside the tile
+  uint32_t w[32];
+  uint32_t m = 0;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    w[r] = *reinterpret_cast<const uint32_t*>(&tile[(kb * 32 + r) * VQ_PITCH + dp * 4]);
+    uint32_t a = w[r] & 0x7FFF7FFFu;
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
+  }
+  float inv0, inv1;
+  const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0);
+  const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1);
+  uint32_t o0[8], o1[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t lo0 = cvt_e4m3x2(bf16_lo(w[4 * i]) * inv0, bf16_lo(w[4 * i + 1]) * inv0);
+    uint32_t hi0 = cvt_e4m3x2(bf16_lo(w[4 * i + 2]) * inv0, bf16_lo(w[4 * i + 3]) * inv0);
+    uint32_t lo1 = cvt_e4m3x2(bf16_hi(w[4 * i]) * inv1, bf16_hi(w[4 * i + 1]) * inv1);
+    uint32_t hi1 = cvt_e4m3x2(bf16_hi(w[4 * i + 2]) * inv1, bf16_hi(w[4 * i + 3]) * inv1);
+    o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu : (lo0 | (hi0 << 16));
+    o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
+  }
+  const int d0 = 2 * dp, d1 = 2 * dp + 1;
+  uint8_t* row0 = vt + ((long long)plane * 128 + d0) * S + s0 + kb * 32;
+  uint8_t* row1 = vt + ((long long)plane * 128 + d1) * S + s0 + kb * 32;
+  __stcs(reinterpret_cast<uint4*>(row0), make_uint4(o0[0], o0[1], o0[2], o0[3]));
+  __stcs(reinterpret_cast<uint4*>(row0) + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
+  __stcs(reinterpret_cast<uint4*>(row1), make_uint4(o1[0], o1[1], o1[2], o1[3]));
+  __stcs(reinterpret_cast<uint4*>(row1) + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
+  uint8_t* atom = vsc + ((long long)plane * ntiles + tile_idx) * 512;
+  atom[atom_word_offset(d0) + kb] = (uint8_t)sb0;
+  atom[atom_word_offset(d1) + kb] = (uint8_t)sb1;
+}
+
+// ------------------------------------------------------------------------------------------
+cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, int S, int H, int layout,
+                                 cudaStream_t st) {
+  const long long nrows = (long long)B * S * H;
+  const long long chunks = nrows * 16;
+  const unsigned grid = (unsigned)((chunks + 255) / 256);
+  quant_rowwise_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(q), sc,
+                                              nrows, B, S, H, layout);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_v(const void* v, uint8_t* vt, uint8_t* vsc, uint8_t* vtn, uint8_t* vtn_sc, int B, int S,
+                           int H, int layout, cudaStream_t st) {
+  const long long ctas = (long long)B * H * (S / VQ_ROWS);
+  quant_v_kernel<<<(unsigned)ctas, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(v), vt, vsc, vtn, vtn_sc, B, S,
+                                                  H, layout);
+  return cudaGetLastError();
+}
+
+}  // namespace bsc

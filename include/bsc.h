@@ -1,0 +1,156 @@
+/*
+ * bsc.h - C ABI of the leak-free causal MXFP8 attention forward library (libbsc.so, sm_103a).
+ *
+ * The operation: "[PyTorch] Add causal MXFP8 attention without future-token leakage through V
+ * scales" (TransformerEngine PR #3865), Description.  A columnwise MXFP8 V scale is shared by 32
+ * consecutive tokens, so under an ordinary causal mask a later token of a query's own 32-token
+ * block can change how earlier visible V values round.  The method attends keys of completed
+ * 32-token blocks (j < 32*floor(i/32)) in MXFP8 with the columnwise V, attends the query's own
+ * block (at most 32 keys, j <= i) on a token-normalised V copy (one power-of-two amplitude per
+ * token), and merges the two partials through their log-sum-exps, so output row i never depends
+ * on a token after i.
+ *
+ * Conventions for every call:
+ *   - Every buffer is device memory owned by the caller.  The library never allocates, frees or
+ *     synchronises; all work is enqueued on `stream` (NULL = the legacy default stream).
+ *   - Arguments are checked before anything is enqueued; on any error nothing is launched.
+ *   - Calls hold no state between invocations and may be made from several host threads.
+ *   - Tokens S must be a multiple of 128 and D must be 128.  B, S or H equal to 0 is an empty
+ *     problem: the call returns BSC_OK and launches nothing (pointers are not inspected).
+ *   - Every pointer must be 16-byte aligned.
+ *   - The current CUDA device must be compute capability 10.3 (GB300).
+ *   - Inputs are assumed finite; a NaN/Inf V value in a later token can reach earlier rows
+ *     through a 0 * NaN product inside the diagonal key tile.
+ *
+ * Data layouts (BSHD: [B][S][H][D]; SBHD: [S][B][H][D]; D fastest in both):
+ *   x_bf16, v_bf16, o_bf16    bf16 in the given layout
+ *   x_e4m3, vtn_e4m3          E4M3 bytes, same layout and strides as the bf16 input
+ *   v_e4m3_t                  E4M3 bytes of V transposed: [B][H][D][S]
+ *   Scale bytes are E8M0 (value 2^(byte-127); 0xFF = NaN) and come in two forms:
+ *   "row atoms" (Q and K rowwise scales):  one byte per (b, h, s, c) with c = d/32, at
+ *        ((b*H + h)*(S/128) + s/128)*512 + (s%32)*16 + ((s%128)/32)*4 + c
+ *   "column atoms" (V columnwise scales): one byte per (b, h, d, 32-token block), at
+ *        ((b*H + h)*(S/128) + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32
+ *     Both are the 128x4 scale-factor atom order read by the tensor cores (each 512-byte atom
+ *     covers 128 rows x 4 blocks of 32), so the attention kernel copies atoms unchanged.
+ *   vtn_sc                    token amplitudes, one byte per (b, h, s) at (b*H + h)*S + s
+ *   lse                       fp32 [B][Hq][S], natural log
+ *
+ * Quantisation rule (OCP MX, E4M3 elements): for a block with maximum magnitude amax, the scale
+ * byte is clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for amax = 0); each element is x*2^-e
+ * rounded to nearest even on the E4M3 grid and saturated to +-448; a block holding NaN/Inf gets
+ * scale 0xFF and element bytes 0x7F.
+ */
+#ifndef BSC_H
+#define BSC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stream handle: a cudaStream_t. */
+typedef struct CUstream_st* bsc_stream_t;
+
+typedef enum {
+  BSC_OK = 0,
+  BSC_ERR_NULL = 1,           /* a required pointer is NULL */
+  BSC_ERR_SHAPE = 2,          /* negative size, Hq not a multiple of Hkv, bad layout code */
+  BSC_ERR_ALIGN = 3,          /* a pointer is not 16-byte aligned */
+  BSC_ERR_UNSUPPORTED = 4,    /* D != 128, S % 128 != 0, wrong device, unsupported option */
+  BSC_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed (launch, tensor map) */
+  BSC_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait gave up (see bsc_read_device_status) */
+} bsc_status;
+
+typedef enum { BSC_BSHD = 0, BSC_SBHD = 1 } bsc_layout;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int bsc_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* bsc_status_string(bsc_status s);
+
+/*
+ * Rowwise MXFP8 quantisation of Q or K: one E8M0 scale per 32 consecutive elements along D of
+ * each (b, s, h) row ("Q/K decoded from their rowwise MXFP8 bytes", PR #3865 Description).
+ *   x_bf16 [in]  bf16 in `layout`;  x_e4m3 [out] same layout;  x_sc [out] row atoms,
+ *   B*H*S*4 bytes.
+ */
+bsc_status mxfp8_quantize_qk_rowwise(const void* x_bf16, int B, int S, int H, int D, bsc_layout layout,
+                                     uint8_t* x_e4m3, uint8_t* x_sc, bsc_stream_t stream);
+
+/*
+ * Columnwise MXFP8 quantisation of V: one E8M0 scale per 32 consecutive tokens of each (b, h, d)
+ * ("A columnwise MXFP8 V scale is shared by 32 consecutive tokens", PR #3865 Description).
+ *   v_bf16 [in] bf16 in `layout`;  v_e4m3_t [out] [B][H][D][S];  v_sc [out] column atoms,
+ *   B*H*(S/32)*D bytes.
+ */
+bsc_status mxfp8_quantize_v_colwise(const void* v_bf16, int B, int S, int H, int D, bsc_layout layout,
+                                    uint8_t* v_e4m3_t, uint8_t* v_sc, bsc_stream_t stream);
+
+/*
+ * Token-normalised V copy: one power-of-two amplitude per (b, s, h) token row ("a
+ * token-normalized copy of V (one power-of-two amplitude per token)", PR #3865 Description),
+ * chosen by the same MX rule with the block spanning all D elements of the row.
+ *   v_bf16 [in];  vtn_e4m3 [out] same layout as V;  vtn_sc [out] B*H*S bytes.
+ */
+bsc_status v_token_normalize(const void* v_bf16, int B, int S, int H, int D, bsc_layout layout,
+                             uint8_t* vtn_e4m3, uint8_t* vtn_sc, bsc_stream_t stream);
+
+/* Both V quantisations in one pass over V (one read); outputs as in the two calls above. */
+bsc_status mxfp8_quantize_v_fused(const void* v_bf16, int B, int S, int H, int D, bsc_layout layout,
+                                  uint8_t* v_e4m3_t, uint8_t* v_sc, uint8_t* vtn_e4m3, uint8_t* vtn_sc,
+                                  bsc_stream_t stream);
+
+typedef struct {
+  const uint8_t* q;       /* [in] Q E4M3 bytes, `layout`, Hq heads */
+  const uint8_t* q_sc;    /* [in] Q row atoms */
+  const uint8_t* k;       /* [in] K E4M3 bytes, `layout`, Hkv heads */
+  const uint8_t* k_sc;    /* [in] K row atoms */
+  const uint8_t* v_t;     /* [in] V columnwise E4M3 bytes, [B][Hkv][D][S] */
+  const uint8_t* v_sc;    /* [in] V column atoms */
+  const uint8_t* vtn;     /* [in] token-normalised V bytes, `layout` (unused when leaky = 1) */
+  const uint8_t* vtn_sc;  /* [in] token amplitudes [B][Hkv][S] (unused when leaky = 1) */
+  void* o;                /* [out] bf16 O in `layout`, Hq heads */
+  float* lse;             /* [out] [B][Hq][S], ln sum_{j<=i} exp(softmax_scale * q_i . k_j) */
+  int B, S, Hq, Hkv, D;
+  int layout;             /* bsc_layout */
+  float softmax_scale;
+  /* Number of E4M3 terms P is split into for the MXFP8 P.V of completed blocks (1 or 2).  P is
+   * quantised after the running-max subtraction with a constant scale (2^-8; the second term
+   * carries the residual at 2^-12), so the scale never depends on data.  The own block uses the
+   * same number of BF16 terms. */
+  int p_terms;
+  /* 0: the method.  1: ordinary (leaky) causal MXFP8 - the own block is attended with the
+   * columnwise V as well; a control that shows the leak. */
+  int leaky;
+  /* Optional device int32 (may be NULL).  Left untouched on success; a device-side wait that
+   * gives up writes 0x100 | site.  Clear it before the call when you intend to read it. */
+  int32_t* dev_status;
+  /* Wall-clock limit of any single device-side wait, milliseconds (0 = 2000). */
+  uint32_t wait_timeout_ms;
+  /* Test hook: 1 makes the MMA issuer wait on a barrier nothing arrives on, so the call ends
+   * through the wait limit with dev_status set.  Must be 0 in normal use. */
+  int debug_stall;
+} bsc_attn_fwd_params;
+
+/*
+ * Leak-free causal MXFP8 attention forward (PR #3865 Description: completed-block MXFP8 part,
+ * own-block part on the token-normalised V, log-sum-exp merge).  GQA: query head h reads
+ * KV head h / (Hq/Hkv).  Returns BF16 O and fp32 LSE.
+ */
+bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the int32 at `dev_status` and returns BSC_OK (0) or
+ * BSC_ERR_DEVICE_TIMEOUT (non-zero).  The only call that synchronises.
+ */
+bsc_status bsc_read_device_status(const int32_t* dev_status, bsc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSC_H */

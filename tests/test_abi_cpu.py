@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports every function include/bsc.h declares, and rejects bad
+arguments with the documented status before touching any device (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsc.h")
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from block_scaled_causal_gb300 import build
+    if not os.path.exists(build.LIB_PATH):
+        build.build()
+    from block_scaled_causal_gb300 import _binding
+    return _binding
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(ops):
+    names = _declared_functions()
+    assert {"mxfp8_quantize_qk_rowwise", "mxfp8_quantize_v_colwise", "v_token_normalize",
+            "mxfp8_quantize_v_fused", "mxfp8_causal_attn_fwd", "bsc_status_string",
+            "bsc_read_device_status", "bsc_abi_version"} <= set(names)
+    lib = ctypes.CDLL(ops._build.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(ops):
+    for code in range(7):
+        assert ops.lib.bsc_status_string(code).decode().startswith("BSC_")
+    assert ops.lib.bsc_abi_version() == 1
+
+
+def test_params_struct_layout(ops):
+    # 10 pointers, 5 ints, layout, float, 2 ints, pointer, uint32, int  (x86-64 / aarch64 LP64)
+    P = ops.AttnFwdParams
+    assert P.B.offset == 80 and P.softmax_scale.offset == 104 and P.dev_status.offset == 120
+    assert ctypes.sizeof(P) == 136
+
+
+FAKE = 0x100000   # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, 1, 128, 2, 64, 0, FAKE, FAKE), 4),       # D != 128
+    ((FAKE, 1, 100, 2, 128, 0, FAKE, FAKE), 4),      # S % 128
+    ((FAKE, -1, 128, 2, 128, 0, FAKE, FAKE), 2),     # negative size
+    ((FAKE, 1, 128, 2, 128, 7, FAKE, FAKE), 2),      # bad layout
+    ((None, 1, 128, 2, 128, 0, FAKE, FAKE), 1),      # NULL input
+    ((FAKE + 8, 1, 128, 2, 128, 0, FAKE, FAKE), 3),  # misaligned
+    ((None, 0, 128, 2, 128, 0, None, None), 0),      # empty problem: nothing to do
+])
+def test_rowwise_validation(ops, args, want):
+    st = ops.lib.mxfp8_quantize_qk_rowwise(*args, None)
+    assert st == want
+
+
+def test_v_validation(ops):
+    L = ops.lib
+    assert L.mxfp8_quantize_v_fused(FAKE, 1, 128, 2, 128, 0, FAKE, FAKE, None, FAKE, None) == 1
+    assert L.mxfp8_quantize_v_colwise(FAKE, 1, 128, 2, 128, 0, FAKE + 4, FAKE, None) == 3
+    assert L.v_token_normalize(FAKE, 1, 96, 2, 128, 0, FAKE, FAKE, None) == 4
+    assert L.v_token_normalize(FAKE, 2, 0, 2, 128, 1, None, None, None) == 0
+
+
+def _params(ops, **kw):
+    base = dict(q=FAKE, q_sc=FAKE, k=FAKE, k_sc=FAKE, v_t=FAKE, v_sc=FAKE, vtn=FAKE, vtn_sc=FAKE, o=FAKE,
+                lse=FAKE, B=1, S=256, Hq=4, Hkv=2, D=128, layout=0, softmax_scale=0.088, p_terms=1, leaky=0,
+                dev_status=0, wait_timeout_ms=0, debug_stall=0)
+    base.update(kw)
+    return ops.AttnFwdParams(**base)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(Hq=3, Hkv=2), 2),
+    (dict(Hkv=0), 2),
+    (dict(D=64), 4),
+    (dict(S=200), 4),
+    (dict(p_terms=3), 4),
+    (dict(leaky=2), 4),
+    (dict(layout=2), 2),
+    (dict(o=0), 1),
+    (dict(vtn=0), 1),
+    (dict(lse=FAKE + 4), 3),
+    (dict(dev_status=FAKE + 2), 3),
+    (dict(S=0), 0),
+    (dict(B=0, q=0, k=0), 0),
+])
+def test_attn_validation(ops, kw, want):
+    p = _params(ops, **kw)
+    assert ops.lib.mxfp8_causal_attn_fwd(ctypes.byref(p), None) == want
+
+
+def test_attn_null_params(ops):
+    assert ops.lib.mxfp8_causal_attn_fwd(None, None) == 1
+    assert ops.lib.bsc_read_device_status(None, None) == 1
