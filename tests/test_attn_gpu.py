@@ -1,11 +1,15 @@
 """GPU leak-free causal MXFP8 attention forward against the fp64 oracle, through the C ABI.
 
 Tolerances: O within max-abs 3e-2 and mean-abs 3e-3 of the oracle and LSE within 1e-3 relative,
-P's FP8 rounding being the only allowed difference.  With two E4M3 terms for P (p_terms=2) that
-holds on every workload.  With one term (p_terms=1) it holds on the N(0,1) workloads; on the
-heavy-tailed V workloads one E4M3 term alone moves O by more than 3e-2, so there the test checks
-the bound that follows from the arithmetic instead: per output element
-    |dO| <= 2^-4 * sum_{completed j} p_ij |Vc_jd| + 2^-8 * sum_{own j} p_ij |Vt_jd| + 2^-8 |O| + eps
+P's FP8 rounding being the only allowed difference.  O is returned in BF16, whose own rounding is
+half an ulp = 2^(floor(log2|O|) - 8): more than 3e-2 once |O| >= 8 (heavy-tailed V rows reach
+|O| ~ 20-60).  The max-abs check therefore allows 3e-2 plus half a BF16 ulp of the oracle value.
+With two E4M3 terms for P (p_terms=2) that holds on every workload.  With one term (p_terms=1)
+it holds on the N(0,1) workloads; on the heavy-tailed V workloads one E4M3 term alone moves O by
+more than 3e-2, so there the test checks the bound that follows from the arithmetic instead: per
+output element
+    |dO| <= 2^-4 * sum_{completed j} p_ij |Vc_jd| + 2^-8 * sum_{own j} p_ij |Vt_jd|
+            + half a BF16 ulp of O + eps
 (half an E4M3 mantissa step on each completed-block weight, a BF16 step on each own-block weight
 and the final BF16 rounding of O).
 """
@@ -84,6 +88,12 @@ def _run(ops, w, q, k, v, p_terms, leaky=0):
     return bshd_np(o, w.layout).astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
+def bf16_half_ulp(x):
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a >= 2.0 ** -126, np.ldexp(1.0, (e - 8).astype(np.int64)), 2.0 ** -134)
+
+
 def _compare(Og, Lg, O, L, bound=None):
     err = np.abs(Og - O)
     lse_rel = np.abs(Lg - L) / np.maximum(np.abs(L), 1e-30)
@@ -91,7 +101,8 @@ def _compare(Og, Lg, O, L, bound=None):
     assert np.all(np.isfinite(Og)), info
     assert lse_rel.max() <= LSE_REL, info
     if bound is None:
-        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, info
+        excess = err - (MAX_ABS + bf16_half_ulp(O))
+        assert excess.max() <= 0 and err.mean() <= MEAN_ABS, info + " excess over 3e-2 + half ulp %.3e" % excess.max()
     else:
         bad = err > bound
         assert not bad.any(), info + " worst excess %.3e" % (err - bound).max()
@@ -99,7 +110,7 @@ def _compare(Og, Lg, O, L, bound=None):
 
 
 def _bound(O, Ac, Ao, maxv):
-    return 2.0 ** -4 * Ac + 2.0 ** -8 * Ao + 2.0 ** -8 * np.abs(O) + 1e-4 * maxv + 1e-6
+    return 2.0 ** -4 * Ac + 2.0 ** -8 * Ao + bf16_half_ulp(O) + 1e-4 * maxv + 1e-6
 
 
 @pytest.mark.parametrize("p_terms", [1, 2])
