@@ -72,7 +72,11 @@ enum Bar : uint32_t {
 // TMEM column map
 constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_SFQ = 384, T_SFK = 388, T_SFV = 396, T_SFP = 404;
 
-// P scale bytes: term 0 holds P * 2^8, term 1 the residual * 2^12.
+// Softmax weights are p' = 2^(x - m_used + P_SHIFT) with x - m_used <= RESCALE_LOG2, so
+// p' < 2^8.8 = 445.7 < 448.  P scale bytes: term 0 holds p' (scale 2^-P_SHIFT), term 1 the
+// residual * 16 (scale 2^-(P_SHIFT+4)).
+constexpr float P_SHIFT = 8.0f;
+constexpr float RESCALE_LOG2 = 0.8f;
 constexpr uint8_t SFP_TERM0 = 127 - 8;
 constexpr uint8_t SFP_TERM1 = 127 - 12;
 
@@ -86,6 +90,7 @@ __device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
   return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);   // 2^(sb-127), sb <= 254
 }
 
+template <int P_TERMS, bool LEAKY>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int t = T - 1 - (int)(blockIdx.x / (a.B * a.Hq));
   const int hq = bh % a.Hq, b = bh / a.Hq;
   const int hk = hq / (a.Hq / a.Hkv);
-  const bool own_split = !a.leaky;
+  constexpr bool own_split = !LEAKY;
 
   // ---- setup
   if (threadIdx.x == 0) {
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!mbar_wait(bar(B_P_FULL + st), n & 1, ctl, W_MMA_P)) return false;
         tc_fence_after();
         tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * st, desc_sf_block(sbase + OFF_SFV + st * 512));
-        for (int term = 0; term < a.p_terms; ++term) {
+        for (int term = 0; term < P_TERMS; ++term) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             mma_mxf8_ts(tO, tS[st] + term * 32 + kk * 8,
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (jj == t && own_split) {
           if (!mbar_wait(bar(B_VT_READY), 0, ctl, W_MMA_VT)) return false;
           tc_fence_after();
-          for (int term = 0; term < a.p_terms; ++term) {
+          for (int term = 0; term < P_TERMS; ++term) {
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
               mma_f16_ts(tO, tS[st ^ 1] + term * 64 + s * 8,
@@ -279,129 +284,150 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int i = t * BM + r;           // query token
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sl2 = a.scale_log2e;
-    float m = -INFINITY, l = 0.f;
+    // Exponentials are taken against m_used, a running row maximum (log2 units) that is raised only
+    // when a tile's maximum exceeds it by more than RESCALE_LOG2; O and l are rescaled then.  The
+    // weights p' = 2^(x - m_used + P_SHIFT) stay below 2^(P_SHIFT + RESCALE_LOG2) < 448, inside the
+    // E4M3 range, and every decision depends only on this row's visible scores.
+    float m_used = -INFINITY;
+    float2 lacc[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) lacc[g] = make_float2(0.f, 0.f);
     bool ok = true;
+#define SV(c) s[(c) >> 5][(c) & 31]
     for (int j = 0; j <= t; ++j) {
       const int st = j & 1, n = j >> 1;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + st), n & 1, ctl, W_SM_S));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tSb = tmem + (st ? T_S1 : T_S0) + lane_off;
-      float x[128];
+      float s[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tSb + 32 * c, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[32 * c + k] = __uint_as_float(rr[k]) * sl2;
-      }
+      for (int c = 0; c < 4; ++c) tmem_ld32f(tSb + 32 * c, s[c]);
+      tmem_ld_wait();
       const bool diag = (j == t);
       if (diag) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = (c > r) ? -INFINITY : x[c];
+        for (int c = 0; c < 128; ++c) SV(c) = (c > r) ? -INFINITY : SV(c);
       }
-      float mt = x[0];
+      // row maximum of the raw scores in 8 independent chains
+      float mx[8];
 #pragma unroll
-      for (int c = 1; c < 127; c += 2) mt = fmax3(mt, x[c], x[c + 1]);
-      mt = fmaxf(mt, x[127]);
-      const float m_new = fmaxf(m, mt);
-      const bool grow = (j > 0) && (m_new > m);
+      for (int g = 0; g < 8; ++g) {
+        const int c0 = 16 * g;
+        float v = fmax3(SV(c0), SV(c0 + 1), SV(c0 + 2));
+#pragma unroll
+        for (int k = 3; k < 15; k += 2) v = fmax3(v, SV(c0 + k), SV(c0 + k + 1));
+        mx[g] = fmaxf(v, SV(c0 + 15));
+      }
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+      const bool need = mt > m_used + RESCALE_LOG2;      // always true at the first tile
+      const float m_new = need ? mt : m_used;
+      const bool resc = need && (j > 0);
       bool pv_waited = false;
-      if (__any_sync(0xFFFFFFFFu, grow)) {
-        // rescale this warp's O rows (factor 1 for rows whose max did not move): needs PV_{j-1} done
+      if (__any_sync(0xFFFFFFFFu, resc)) {
+        // rescale this warp's O rows (factor 1 where the row keeps its max): needs PV_{j-1} done
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_PV_DONE), (j - 1) & 1, ctl, W_SM_PV));
         if (!ok) break;
         pv_waited = true;
         tc_fence_after();
-        const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+        const float alpha = resc ? ex2_approx(m_used - m_new) : 1.0f;
         const uint32_t tOb = tmem + T_O + lane_off;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tOb + 32 * c, rr);
+        for (int h = 0; h < 2; ++h) {
+          float o0[32], o1[32];
+          tmem_ld32f(tOb + 64 * h, o0);
+          tmem_ld32f(tOb + 64 * h + 32, o1);
           tmem_ld_wait();
+          uint32_t u0[32], u1[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) rr[k] = __float_as_uint(__uint_as_float(rr[k]) * alpha);
-          tmem_st32(tOb + 32 * c, rr);
+          for (int k = 0; k < 32; ++k) {
+            u0[k] = __float_as_uint(o0[k] * alpha);
+            u1[k] = __float_as_uint(o1[k] * alpha);
+          }
+          tmem_st32(tOb + 64 * h, u0);
+          tmem_st32(tOb + 64 * h + 32, u1);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          lacc[g].x *= alpha;
+          lacc[g].y *= alpha;
         }
       }
-      const float alpha_l = grow ? ex2_approx(m - m_new) : 1.0f;
-      // p' = 2^(x - m_new + 8) = 256 * p
-      const float mb = m_new - 8.0f;
-      float rowsum = 0.f;
+      m_used = m_new;
+      // p' = 2^(s * scale*log2(e) - m_used + P_SHIFT), two lanes per packed FMA
+      const float2 mul2 = make_float2(sl2, sl2);
+      const float2 add2 = make_float2(P_SHIFT - m_used, P_SHIFT - m_used);
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        x[c] = ex2_approx(x[c] - mb);
-        rowsum += x[c];
+      for (int c = 0; c < 128; c += 2) {
+        const float2 x2 = __ffma2_rn(make_float2(SV(c), SV(c + 1)), mul2, add2);
+        SV(c) = ex2_approx(x2.x);
+        SV(c + 1) = ex2_approx(x2.y);
+        lacc[(c >> 1) & 3] = __fadd2_rn(lacc[(c >> 1) & 3], make_float2(SV(c), SV(c + 1)));
       }
-      l = l * alpha_l + rowsum;
-      m = m_new;
-      // E4M3 P for completed keys; in the diagonal tile keys of the own and later 32-blocks are 0
-      // (the leaky control keeps the own block here instead).
-      const int fp8_limit = diag ? (a.leaky ? q + 1 : q) : 4;   // 32-key blocks kb < limit use this path
-      uint32_t w0[32], w1[32];
+      // E4M3 P for completed keys (scale 2^-P_SHIFT; a second term holds the residual at 2^-4 of
+      // that); in the diagonal tile the own and later 32-key blocks are 0 (the leaky control keeps
+      // the own block on this path instead).
+      const int fp8_limit = diag ? (LEAKY ? q + 1 : q) : 4;
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
         const bool use = kb < fp8_limit;
+        uint32_t w0[8], w1[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const int c = kb * 32 + g * 4;
-          const float p0 = use ? x[c] : 0.f, p1 = use ? x[c + 1] : 0.f;
-          const float p2 = use ? x[c + 2] : 0.f, p3 = use ? x[c + 3] : 0.f;
+          const float p0 = use ? SV(c) : 0.f, p1 = use ? SV(c + 1) : 0.f;
+          const float p2 = use ? SV(c + 2) : 0.f, p3 = use ? SV(c + 3) : 0.f;
           const uint16_t h01 = cvt_e4m3x2(p0, p1), h23 = cvt_e4m3x2(p2, p3);
-          w0[kb * 8 + g] = (uint32_t)h01 | ((uint32_t)h23 << 16);
-          if (a.p_terms > 1) {
+          w0[g] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+          if (P_TERMS > 1) {
             const uint32_t f01 = cvt_e4m3x2_to_f16x2(h01), f23 = cvt_e4m3x2_to_f16x2(h23);
             const float d0 = p0 - __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFFu)));
             const float d1 = p1 - __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
             const float d2 = p2 - __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFFu)));
             const float d3 = p3 - __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
-            w1[kb * 8 + g] = (uint32_t)cvt_e4m3x2(d0 * 16.f, d1 * 16.f) |
-                             ((uint32_t)cvt_e4m3x2(d2 * 16.f, d3 * 16.f) << 16);
+            w1[g] = (uint32_t)cvt_e4m3x2(d0 * 16.f, d1 * 16.f) | ((uint32_t)cvt_e4m3x2(d2 * 16.f, d3 * 16.f) << 16);
           }
         }
+        tmem_st8(tSb + kb * 8, w0);
+        if (P_TERMS > 1) tmem_st8(tSb + 32 + kb * 8, w1);
       }
-      tmem_st32(tSb, w0);
-      if (a.p_terms > 1) tmem_st32(tSb + 32, w1);
-      if (diag && own_split) {
-        // own block (keys of sub-block q, j <= i) as BF16 P (1 or 2 terms) into the other S buffer,
-        // which PV_{t-1} may still be reading
+      if (diag && !LEAKY) {
+        // own block (keys of sub-block q, j <= i) as BF16 P (P_TERMS terms) into the other S
+        // buffer, which PV_{t-1} may still be reading
         if (t > 0 && !pv_waited) {
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_PV_DONE), (t - 1) & 1, ctl, W_SM_PV));
           if (!ok) break;
           tc_fence_after();
         }
         const uint32_t tPo = tmem + (st ? T_S0 : T_S1) + lane_off;
-        uint32_t hi[32], lo[32];
+        const float unshift = 1.0f / (float)(1 << (int)P_SHIFT);
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
+          uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = kb * 32 + 2 * e;
-            const float p0 = (kb == q) ? x[c] * (1.0f / 256.0f) : 0.f;
-            const float p1 = (kb == q) ? x[c + 1] * (1.0f / 256.0f) : 0.f;
-            const uint32_t h = pack_bf16x2(p0, p1);
-            const float r0 = p0 - __uint_as_float(h << 16), r1 = p1 - __uint_as_float(h & 0xFFFF0000u);
-            const int idx = (kb & 1) * 16 + e;
-            hi[idx] = h;
-            lo[idx] = pack_bf16x2(r0, r1);
+            const float p0 = (kb == q) ? SV(c) * unshift : 0.f;
+            const float p1 = (kb == q) ? SV(c + 1) * unshift : 0.f;
+            hi[e] = pack_bf16x2(p0, p1);
+            lo[e] = pack_bf16x2(p0 - __uint_as_float(hi[e] << 16), p1 - __uint_as_float(hi[e] & 0xFFFF0000u));
           }
-          if (kb & 1) {
-            tmem_st32(tPo + (kb >> 1) * 32, hi);
-            if (a.p_terms > 1) tmem_st32(tPo + 64 + (kb >> 1) * 32, lo);
-          }
+          tmem_st16(tPo + kb * 16, hi);
+          if (P_TERMS > 1) tmem_st16(tPo + 64 + kb * 16, lo);
         }
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL + st));
     }
+#undef SV
     // ---- epilogue: O / l -> BF16, LSE (natural log)
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_O_FULL), 0, ctl, W_SM_O));
     if (ok) {
       tc_fence_after();
-      const float inv_l = 256.0f / l;
+      const float l = ((lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y)) +
+                      ((lacc[2].x + lacc[2].y) + (lacc[3].x + lacc[3].y));
+      const float inv_l = (float)(1 << (int)P_SHIFT) / l;
       const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq
                                           : ((long long)i * a.B + b) * a.Hq + hq;
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + row * HD);
@@ -423,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       const float ln2 = 0.69314718055994531f;
-      a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m + lg2_approx(l) - 8.0f) * ln2;
+      a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m_used + lg2_approx(l) - P_SHIFT) * ln2;
     }
   }
 
@@ -434,18 +460,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-}  // namespace
-
-cudaError_t launch_attn_fwd(const AttnArgs& args, cudaStream_t st) {
-  static bool attr_set = false;   // per-process; the attribute is per function
+template <int P_TERMS, bool LEAKY>
+cudaError_t launch_variant(const AttnArgs& args, cudaStream_t st) {
+  static bool attr_set = false;   // the attribute is per function and per process
+  auto kern = attn_fwd_kernel<P_TERMS, LEAKY>;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const long long ctas = (long long)args.B * args.Hq * (args.S / BM);
-  attn_fwd_kernel<<<(unsigned)ctas, kThreads, SMEM_BYTES, st>>>(args);
+  kern<<<(unsigned)ctas, kThreads, SMEM_BYTES, st>>>(args);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnArgs& args, cudaStream_t st) {
+  if (args.p_terms == 2) return args.leaky ? launch_variant<2, true>(args, st) : launch_variant<2, false>(args, st);
+  return args.leaky ? launch_variant<1, true>(args, st) : launch_variant<1, false>(args, st);
 }
 
 }  // namespace bsc
