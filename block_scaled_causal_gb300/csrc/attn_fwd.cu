@@ -10,12 +10,14 @@
 // done incrementally, and both P.V products accumulate into one fp32 O accumulator in TMEM.
 //
 // One CTA computes one 128-row query tile t of one (batch, query head) and walks key tiles 0..t.
-// Warp roles (256 threads):
-//   warp 0     TMA producer: Q tile + scales once; K, V (columnwise, transposed) tiles + scales
-//              through a 2-stage ring; the own-block token-normalised V tile once.
-//   warp 1     allocates TMEM; lane 0 issues tcgen05.cp (scale factors) and tcgen05.mma.
-//   warps 2-3  decode the token-normalised V tile to BF16 (exact) in the MMA operand layout.
-//   warps 4-7  softmax, one query row per thread (TMEM lane = row), then the epilogue.
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q tile + scales once; K, V (columnwise, transposed) tiles + scales
+//               through a 4-stage ring; the own-block token-normalised V tile once.
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.cp (scale factors) and tcgen05.mma.
+//   warps 2-3   decode the token-normalised V tile to BF16 (exact) in the MMA operand layout.
+//   warps 4-11  softmax: two warpgroups, each owning one 64-column half of every S row (warps 4+q
+//               and 8+q share TMEM lane quarter q = query rows 32q..32q+31); the row maximum is
+//               exchanged through shared memory once per key tile.  Then the epilogue.
 // TMEM (512 columns): S[0] 0-127, S[1] 128-255, O 256-383, scale factors from 384.
 // P (E4M3, 32 columns per term) is written over the S buffer it came from; the own-block BF16 P
 // goes to the other S buffer.
@@ -34,40 +36,46 @@ namespace {
 constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // keys per tile
 constexpr int HD = 128;   // head dimension
-constexpr int kThreads = 256;
+constexpr int NST = 4;    // K/V shared-memory stages
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + BM * HD;             // 2 stages
-constexpr uint32_t OFF_V = OFF_K + 2 * BN * HD;         // 2 stages (d rows x 128 keys)
-constexpr uint32_t OFF_VT = OFF_V + 2 * HD * BN;        // own-block V, BF16, 2 K-atoms of 16 KB
-constexpr uint32_t OFF_VTN8 = OFF_VT + 2 * HD * BN;     // raw token-normalised bytes [key][d]
+constexpr uint32_t OFF_K = OFF_Q + BM * HD;              // NST stages, 128 keys x 128 d
+constexpr uint32_t OFF_V = OFF_K + NST * BN * HD;        // NST stages, 128 d rows x 128 keys
+constexpr uint32_t OFF_VT = OFF_V + NST * HD * BN;       // own-block V, BF16, 2 K-atoms of 16 KB
+constexpr uint32_t OFF_VTN8 = OFF_VT + 2 * HD * BN;      // raw token-normalised bytes [key][d]
 constexpr uint32_t OFF_SFQ = OFF_VTN8 + BN * HD;
-constexpr uint32_t OFF_SFK = OFF_SFQ + 512;             // 2 stages
-constexpr uint32_t OFF_SFV = OFF_SFK + 2 * 512;         // 2 stages
-constexpr uint32_t OFF_SFP = OFF_SFV + 2 * 512;         // P scale blocks: term 0, term 1
-constexpr uint32_t OFF_VTNSC = OFF_SFP + 2 * 512;       // 128 token amplitudes
-constexpr uint32_t OFF_BAR = OFF_VTNSC + 128;
-constexpr uint32_t NUM_BARS = 20;
-constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem slot, abort flag
+constexpr uint32_t OFF_SFK = OFF_SFQ + 512;              // NST stages
+constexpr uint32_t OFF_SFV = OFF_SFK + NST * 512;        // NST stages
+constexpr uint32_t OFF_SFP = OFF_SFV + NST * 512;        // P scale blocks: term 0, term 1
+constexpr uint32_t OFF_VTNSC = OFF_SFP + 2 * 512;        // 128 token amplitudes
+constexpr uint32_t OFF_RED = OFF_VTNSC + 128;            // float [2 parity][2 halves][128 rows] maxima
+constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4; // float [2 halves][128 rows] row sums
+constexpr uint32_t OFF_BAR = OFF_REDL + 2 * 128 * 4;
+constexpr uint32_t NUM_BARS = 32;
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;    // tmem slot, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // alignment slack
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;        // alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
+// A stage holds K_j and V_j with their scales: FULL[st] completes when the copies land, FREE[st]
+// when PV_j (the last reader) completes; FREE also tells the softmax that PV_j is done.
 enum Bar : uint32_t {
   B_Q_FULL = 0,
-  B_K_FULL = 1,    // +stage
-  B_K_EMPTY = 3,   // +stage
-  B_V_FULL = 5,    // +stage
-  B_V_EMPTY = 7,   // +stage
-  B_S_FULL = 9,    // +buffer
-  B_P_FULL = 11,   // +buffer
-  B_PV_DONE = 13,
-  B_O_FULL = 14,
-  B_VTN_FULL = 15,
-  B_VT_READY = 16,
-  B_DRAIN = 17,
-  B_INJECT = 18,
+  B_FULL = 1,                    // + stage
+  B_FREE = B_FULL + NST,         // + stage
+  B_S_FULL = B_FREE + NST,       // + S buffer
+  B_P_FULL = B_S_FULL + 2,       // + S buffer
+  B_O_FULL = B_P_FULL + 2,
+  B_VTN_FULL,
+  B_VT_READY,
+  B_DRAIN,
+  B_INJECT,
+  B_COUNT,
 };
+static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
 // TMEM column map
 constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_SFQ = 384, T_SFK = 388, T_SFV = 396, T_SFP = 404;
@@ -82,12 +90,17 @@ constexpr uint8_t SFP_TERM1 = 127 - 12;
 
 // wait-site codes reported through the device status word
 enum Site : int {
-  W_PROD_KEMPTY = 1, W_PROD_VEMPTY, W_MMA_Q, W_MMA_K, W_MMA_V, W_MMA_P, W_MMA_VT, W_MMA_INJECT,
+  W_PROD_FREE = 1, W_MMA_Q, W_MMA_KV, W_MMA_P, W_MMA_VT, W_MMA_INJECT,
   W_SM_S, W_SM_PV, W_SM_O, W_DEC_VTN,
 };
 
 __device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
   return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);   // 2^(sb-127), sb <= 254
+}
+
+// Named barrier for the two softmax warps that share a TMEM lane quarter.
+__device__ __forceinline__ void pair_sync(int q) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
 }
 
 template <int P_TERMS, bool LEAKY>
@@ -111,15 +124,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // ---- setup
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_K_FULL + s), 1);
-      mbar_init(bar(B_K_EMPTY + s), 1);
-      mbar_init(bar(B_V_FULL + s), 1);
-      mbar_init(bar(B_V_EMPTY + s), 1);
-      mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_P_FULL + s), 128);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_FREE + s), 1);
     }
-    mbar_init(bar(B_PV_DONE), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_S_FULL + s), 1);
+      mbar_init(bar(B_P_FULL + s), kSoftmaxThreads);
+    }
     mbar_init(bar(B_O_FULL), 1);
     mbar_init(bar(B_VTN_FULL), 1);
     mbar_init(bar(B_VT_READY), 64);
@@ -153,20 +165,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_arrive_expect_tx(bar(B_Q_FULL), BM * HD + 512);
       tma_load_4d(sbase + OFF_Q, &a.tm_q, bar(B_Q_FULL), 0, hq, t * BM, b);
       bulk_load(sbase + OFF_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + t) * 512, 512, bar(B_Q_FULL));
-      int nk[2] = {0, 0}, nv[2] = {0, 0};   // loads issued per stage
+      int nl[NST] = {};   // stage loads issued
       bool ok = true;
       for (int j = 0; j <= t && ok; ++j) {
-        const int st = j & 1, n = j >> 1;
-        if (n > 0 && !(ok = mbar_wait(bar(B_K_EMPTY + st), (n - 1) & 1, ctl, W_PROD_KEMPTY))) break;
-        mbar_arrive_expect_tx(bar(B_K_FULL + st), BN * HD + 512);
-        tma_load_4d(sbase + OFF_K + st * BN * HD, &a.tm_k, bar(B_K_FULL + st), 0, hk, j * BN, b);
-        bulk_load(sbase + OFF_SFK + st * 512, a.k_sc + (kv_plane * T + j) * 512, 512, bar(B_K_FULL + st));
-        ++nk[st];
-        if (n > 0 && !(ok = mbar_wait(bar(B_V_EMPTY + st), (n - 1) & 1, ctl, W_PROD_VEMPTY))) break;
-        mbar_arrive_expect_tx(bar(B_V_FULL + st), HD * BN + 512);
-        tma_load_2d(sbase + OFF_V + st * HD * BN, &a.tm_v, bar(B_V_FULL + st), j * BN, (int)(kv_plane * HD));
-        bulk_load(sbase + OFF_SFV + st * 512, a.v_sc + (kv_plane * T + j) * 512, 512, bar(B_V_FULL + st));
-        ++nv[st];
+        const int st = j % NST, n = j / NST;
+        if (n > 0 && !(ok = mbar_wait(bar(B_FREE + st), (n - 1) & 1, ctl, W_PROD_FREE))) break;
+        mbar_arrive_expect_tx(bar(B_FULL + st), 2 * BN * HD + 1024);
+        tma_load_4d(sbase + OFF_K + st * BN * HD, &a.tm_k, bar(B_FULL + st), 0, hk, j * BN, b);
+        bulk_load(sbase + OFF_SFK + st * 512, a.k_sc + (kv_plane * T + j) * 512, 512, bar(B_FULL + st));
+        tma_load_2d(sbase + OFF_V + st * HD * BN, &a.tm_v, bar(B_FULL + st), j * BN, (int)(kv_plane * HD));
+        bulk_load(sbase + OFF_SFV + st * 512, a.v_sc + (kv_plane * T + j) * 512, 512, bar(B_FULL + st));
+        ++nl[st];
       }
       bool vtn_issued = false;
       if (own_split && ok) {
@@ -177,9 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         vtn_issued = true;
       }
       // drain: every copy this thread issued must land before the CTA may exit
-      for (int st = 0; st < 2; ++st) {
-        if (nk[st] > 0) mbar_wait_drain(bar(B_K_FULL + st), (nk[st] - 1) & 1, a.limit_ns);
-        if (nv[st] > 0) mbar_wait_drain(bar(B_V_FULL + st), (nv[st] - 1) & 1, a.limit_ns);
+      for (int st = 0; st < NST; ++st) {
+        if (nl[st] > 0) mbar_wait_drain(bar(B_FULL + st), (nl[st] - 1) & 1, a.limit_ns);
       }
       mbar_wait_drain(bar(B_Q_FULL), 0, a.limit_ns);
       if (vtn_issued) mbar_wait_drain(bar(B_VTN_FULL), 0, a.limit_ns);
@@ -198,52 +206,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_cp_32x128b_warpx4(tmem + T_SFP, desc_sf_block(sbase + OFF_SFP));
         tc_cp_32x128b_warpx4(tmem + T_SFP + 4, desc_sf_block(sbase + OFF_SFP + 512));
       }
-      auto pv = [&](int jj) -> bool {
-        const int st = jj & 1, n = jj >> 1;
-        if (!mbar_wait(bar(B_V_FULL + st), n & 1, ctl, W_MMA_V)) return false;
-        if (!mbar_wait(bar(B_P_FULL + st), n & 1, ctl, W_MMA_P)) return false;
-        tc_fence_after();
-        tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * st, desc_sf_block(sbase + OFF_SFV + st * 512));
-        for (int term = 0; term < P_TERMS; ++term) {
+      // Per key tile j: wait for stage j, copy its K and V scale atoms to TMEM, S_j = Q K_j^T;
+      // then O += P_{j-1} V_{j-1} once the softmax has written P_{j-1} (the own block follows in
+      // the diagonal tile).  Everything one thread issues executes in order.
+      for (int jj = 0; jj <= t + 1 && ok; ++jj) {
+        if (jj <= t) {
+          const int j = jj, st = j % NST, sb = j & 1;
+          if (!(ok = mbar_wait(bar(B_FULL + st), (j / NST) & 1, ctl, W_MMA_KV))) break;
+          tc_fence_after();
+          tc_cp_32x128b_warpx4(tmem + T_SFK + 4 * sb, desc_sf_block(sbase + OFF_SFK + st * 512));
+          tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * sb, desc_sf_block(sbase + OFF_SFV + st * 512));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8_ts(tO, tS[st] + term * 32 + kk * 8,
-                        desc_kmajor_sw128(sbase + OFF_V + st * HD * BN + kk * 32), idesc_mxf8(BM, HD, kk, kk),
-                        tmem + T_SFP + 4 * term, tmem + T_SFV + 4 * st, (jj > 0 || term > 0 || kk > 0) ? 1u : 0u);
+            mma_mxf8_ss(tS[sb], desc_kmajor_sw128(sbase + OFF_Q + kk * 32),
+                        desc_kmajor_sw128(sbase + OFF_K + st * BN * HD + kk * 32), idesc_mxf8(BM, BN, kk, kk),
+                        tmem + T_SFQ, tmem + T_SFK + 4 * sb, kk > 0 ? 1u : 0u);
           }
+          tc_commit(bar(B_S_FULL + sb));
         }
-        if (jj == t && own_split) {
-          if (!mbar_wait(bar(B_VT_READY), 0, ctl, W_MMA_VT)) return false;
+        if (jj >= 1) {
+          const int j = jj - 1, st = j % NST, sb = j & 1;
+          if (!(ok = mbar_wait(bar(B_P_FULL + sb), (j >> 1) & 1, ctl, W_MMA_P))) break;
           tc_fence_after();
+#pragma unroll
           for (int term = 0; term < P_TERMS; ++term) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-              mma_f16_ts(tO, tS[st ^ 1] + term * 64 + s * 8,
-                         desc_kmajor_sw128(sbase + OFF_VT + (s >> 2) * (HD * 128) + (s & 3) * 32),
-                         idesc_bf16(BM, HD), 1u);
+            for (int kk = 0; kk < 4; ++kk) {
+              mma_mxf8_ts(tO, tS[sb] + term * 32 + kk * 8,
+                          desc_kmajor_sw128(sbase + OFF_V + st * HD * BN + kk * 32), idesc_mxf8(BM, HD, kk, kk),
+                          tmem + T_SFP + 4 * term, tmem + T_SFV + 4 * sb, (j > 0 || term > 0 || kk > 0) ? 1u : 0u);
             }
           }
-        }
-        tc_commit(bar(B_V_EMPTY + st));
-        tc_commit(bar(B_PV_DONE));
-        return true;
-      };
-      for (int j = 0; j <= t && ok; ++j) {
-        const int st = j & 1, n = j >> 1;
-        if (!(ok = mbar_wait(bar(B_K_FULL + st), n & 1, ctl, W_MMA_K))) break;
-        tc_fence_after();
-        tc_cp_32x128b_warpx4(tmem + T_SFK + 4 * st, desc_sf_block(sbase + OFF_SFK + st * 512));
+          if (j == t && own_split) {
+            if (!(ok = mbar_wait(bar(B_VT_READY), 0, ctl, W_MMA_VT))) break;
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          mma_mxf8_ss(tS[st], desc_kmajor_sw128(sbase + OFF_Q + kk * 32),
-                      desc_kmajor_sw128(sbase + OFF_K + st * BN * HD + kk * 32), idesc_mxf8(BM, BN, kk, kk),
-                      tmem + T_SFQ, tmem + T_SFK + 4 * st, kk > 0 ? 1u : 0u);
+            for (int term = 0; term < P_TERMS; ++term) {
+#pragma unroll
+              for (int s = 0; s < 8; ++s) {
+                mma_f16_ts(tO, tS[sb ^ 1] + term * 64 + s * 8,
+                           desc_kmajor_sw128(sbase + OFF_VT + (s >> 2) * (HD * 128) + (s & 3) * 32),
+                           idesc_bf16(BM, HD), 1u);
+              }
+            }
+          }
+          tc_commit(bar(B_FREE + st));
         }
-        tc_commit(bar(B_S_FULL + st));
-        tc_commit(bar(B_K_EMPTY + st));
-        if (j >= 1) ok = pv(j - 1);
       }
-      if (ok) ok = pv(t);
       if (ok) tc_commit(bar(B_O_FULL));
       // drain every tcgen05 operation this thread issued before TMEM is released
       tc_commit(bar(B_DRAIN));
@@ -278,12 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_arrive(bar(B_VT_READY));
     }
   } else {
-    // ======================= softmax + epilogue (128 threads, one row each)
-    const int q = warp - 4;             // TMEM lane quarter == 32-row query sub-block of the tile
+    // ======================= softmax + epilogue (256 threads: row r, column half h)
+    const int q = warp & 3;             // TMEM lane quarter == 32-row query sub-block of the tile
+    const int h = (warp - 4) >> 2;      // column half: keys / O columns [64h, 64h + 64)
     const int r = q * 32 + lane;        // row inside the tile
     const int i = t * BM + r;           // query token
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sl2 = a.scale_log2e;
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);     // [parity][half][row]
+    float* redl = reinterpret_cast<float*>(smem + OFF_REDL);   // [half][row]
     // Exponentials are taken against m_used, a running row maximum (log2 units) that is raised only
     // when a tile's maximum exceeds it by more than RESCALE_LOG2; O and l are rescaled then.  The
     // weights p' = 2^(x - m_used + P_SHIFT) stay below 2^(P_SHIFT + RESCALE_LOG2) < 448, inside the
@@ -295,58 +307,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     bool ok = true;
 #define SV(c) s[(c) >> 5][(c) & 31]
     for (int j = 0; j <= t; ++j) {
-      const int st = j & 1, n = j >> 1;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + st), n & 1, ctl, W_SM_S));
+      const int sb = j & 1;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, ctl, W_SM_S));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tSb = tmem + (st ? T_S1 : T_S0) + lane_off;
-      float s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32f(tSb + 32 * c, s[c]);
+      const uint32_t tSb = tmem + (sb ? T_S1 : T_S0) + lane_off;
+      float s[2][32];   // this thread's 64 scores: keys 64h + c
+      tmem_ld32f(tSb + 64 * h, s[0]);
+      tmem_ld32f(tSb + 64 * h + 32, s[1]);
       tmem_ld_wait();
       const bool diag = (j == t);
       if (diag) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) SV(c) = (c > r) ? -INFINITY : SV(c);
+        for (int c = 0; c < 64; ++c) SV(c) = (64 * h + c > r) ? -INFINITY : SV(c);
       }
-      // row maximum of the raw scores in 8 independent chains
-      float mx[8];
+      // partial row maximum of the raw scores in 4 independent chains, exchanged with the partner
+      float mx[4];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
+      for (int g = 0; g < 4; ++g) {
         const int c0 = 16 * g;
         float v = fmax3(SV(c0), SV(c0 + 1), SV(c0 + 2));
 #pragma unroll
         for (int k = 3; k < 15; k += 2) v = fmax3(v, SV(c0 + k), SV(c0 + k + 1));
         mx[g] = fmaxf(v, SV(c0 + 15));
       }
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+      const float pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      red[(sb * 2 + h) * 128 + r] = pm;
+      pair_sync(q);
+      const float mt = fmaxf(red[(sb * 2 + 0) * 128 + r], red[(sb * 2 + 1) * 128 + r]) * sl2;
       const bool need = mt > m_used + RESCALE_LOG2;      // always true at the first tile
       const float m_new = need ? mt : m_used;
       const bool resc = need && (j > 0);
       bool pv_waited = false;
       if (__any_sync(0xFFFFFFFFu, resc)) {
-        // rescale this warp's O rows (factor 1 where the row keeps its max): needs PV_{j-1} done
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_PV_DONE), (j - 1) & 1, ctl, W_SM_PV));
+        // rescale this thread's half of its O row (factor 1 where the row keeps its max): needs
+        // PV_{j-1} done
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_FREE + (j - 1) % NST), ((j - 1) / NST) & 1, ctl, W_SM_PV));
         if (!ok) break;
         pv_waited = true;
         tc_fence_after();
         const float alpha = resc ? ex2_approx(m_used - m_new) : 1.0f;
-        const uint32_t tOb = tmem + T_O + lane_off;
+        const uint32_t tOb = tmem + T_O + lane_off + 64 * h;
+        float o0[32], o1[32];
+        tmem_ld32f(tOb, o0);
+        tmem_ld32f(tOb + 32, o1);
+        tmem_ld_wait();
+        uint32_t u0[32], u1[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float o0[32], o1[32];
-          tmem_ld32f(tOb + 64 * h, o0);
-          tmem_ld32f(tOb + 64 * h + 32, o1);
-          tmem_ld_wait();
-          uint32_t u0[32], u1[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            u0[k] = __float_as_uint(o0[k] * alpha);
-            u1[k] = __float_as_uint(o1[k] * alpha);
-          }
-          tmem_st32(tOb + 64 * h, u0);
-          tmem_st32(tOb + 64 * h + 32, u1);
+        for (int k = 0; k < 32; ++k) {
+          u0[k] = __float_as_uint(o0[k] * alpha);
+          u1[k] = __float_as_uint(o1[k] * alpha);
         }
+        tmem_st32(tOb, u0);
+        tmem_st32(tOb + 32, u1);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           lacc[g].x *= alpha;
@@ -358,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const float2 mul2 = make_float2(sl2, sl2);
       const float2 add2 = make_float2(P_SHIFT - m_used, P_SHIFT - m_used);
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
+      for (int c = 0; c < 64; c += 2) {
         const float2 x2 = __ffma2_rn(make_float2(SV(c), SV(c + 1)), mul2, add2);
         SV(c) = ex2_approx(x2.x);
         SV(c + 1) = ex2_approx(x2.y);
@@ -366,15 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       // E4M3 P for completed keys (scale 2^-P_SHIFT; a second term holds the residual at 2^-4 of
       // that); in the diagonal tile the own and later 32-key blocks are 0 (the leaky control keeps
-      // the own block on this path instead).
+      // the own block on this path instead).  Key block kb = 2h + kk of the tile.
       const int fp8_limit = diag ? (LEAKY ? q + 1 : q) : 4;
 #pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
+      for (int kk = 0; kk < 2; ++kk) {
+        const int kb = 2 * h + kk;
         const bool use = kb < fp8_limit;
         uint32_t w0[8], w1[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const int c = kb * 32 + g * 4;
+          const int c = kk * 32 + g * 4;
           const float p0 = use ? SV(c) : 0.f, p1 = use ? SV(c + 1) : 0.f;
           const float p2 = use ? SV(c + 2) : 0.f, p3 = use ? SV(c + 3) : 0.f;
           const uint16_t h01 = cvt_e4m3x2(p0, p1), h23 = cvt_e4m3x2(p2, p3);
@@ -395,18 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // own block (keys of sub-block q, j <= i) as BF16 P (P_TERMS terms) into the other S
         // buffer, which PV_{t-1} may still be reading
         if (t > 0 && !pv_waited) {
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_PV_DONE), (t - 1) & 1, ctl, W_SM_PV));
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_FREE + (t - 1) % NST), ((t - 1) / NST) & 1, ctl, W_SM_PV));
           if (!ok) break;
           tc_fence_after();
         }
-        const uint32_t tPo = tmem + (st ? T_S0 : T_S1) + lane_off;
+        const uint32_t tPo = tmem + (sb ? T_S0 : T_S1) + lane_off;
         const float unshift = 1.0f / (float)(1 << (int)P_SHIFT);
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
+        for (int kk = 0; kk < 2; ++kk) {
+          const int kb = 2 * h + kk;
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int c = kb * 32 + 2 * e;
+            const int c = kk * 32 + 2 * e;
             const float p0 = (kb == q) ? SV(c) * unshift : 0.f;
             const float p1 = (kb == q) ? SV(c + 1) * unshift : 0.f;
             hi[e] = pack_bf16x2(p0, p1);
@@ -418,38 +433,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_P_FULL + st));
+      mbar_arrive(bar(B_P_FULL + sb));
     }
 #undef SV
-    // ---- epilogue: O / l -> BF16, LSE (natural log)
+    // ---- epilogue: O / l -> BF16 (this thread's 64 columns), LSE (natural log)
+    redl[h * 128 + r] = ((lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y)) +
+                        ((lacc[2].x + lacc[2].y) + (lacc[3].x + lacc[3].y));
+    pair_sync(q);
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_O_FULL), 0, ctl, W_SM_O));
     if (ok) {
       tc_fence_after();
-      const float l = ((lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y)) +
-                      ((lacc[2].x + lacc[2].y) + (lacc[3].x + lacc[3].y));
+      const float l = redl[r] + redl[128 + r];
       const float inv_l = (float)(1 << (int)P_SHIFT) / l;
       const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq
                                           : ((long long)i * a.B + b) * a.Hq + hq;
-      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + row * HD);
-      const uint32_t tOb = tmem + T_O + lane_off;
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + row * HD + 64 * h);
+      const uint32_t tOb = tmem + T_O + lane_off + 64 * h;
+      float o[2][32];
+      tmem_ld32f(tOb, o[0]);
+      tmem_ld32f(tOb + 32, o[1]);
+      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tOb + 32 * c, rr);
-        tmem_ld_wait();
+      for (int g = 0; g < 8; ++g) {
+        uint32_t w[4];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = g * 8 + 2 * e;
-            w[e] = pack_bf16x2(__uint_as_float(rr[k]) * inv_l, __uint_as_float(rr[k + 1]) * inv_l);
-          }
-          orow[c * 4 + g] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 4; ++e) {
+          const int k = g * 8 + 2 * e;
+          w[e] = pack_bf16x2(o[k >> 5][k & 31] * inv_l, o[(k + 1) >> 5][(k + 1) & 31] * inv_l);
         }
+        orow[g] = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      const float ln2 = 0.69314718055994531f;
-      a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m_used + lg2_approx(l) - P_SHIFT) * ln2;
+      if (h == 0) {
+        const float ln2 = 0.69314718055994531f;
+        a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m_used + lg2_approx(l) - P_SHIFT) * ln2;
+      }
     }
   }
 

@@ -50,11 +50,20 @@ struct WaitCtl {
   uint64_t limit_ns;
 };
 
-// Bounded wait: returns true once the phase with `parity` has completed; returns false if another
-// thread of the CTA has aborted, or if this wait ran past the limit (then it records `site` in the
-// device status word and raises the CTA's abort flag).
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{.reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Slow path of mbar_wait: bounded by the wall clock.  Returns false if another thread of the CTA
+// has aborted, or if this wait ran past the limit (then it records `site` in the device status
+// word and raises the CTA's abort flag).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -67,6 +76,13 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, con
       }
     }
   }
+}
+
+// Bounded wait for the phase with `parity` of an mbarrier: an inline non-blocking test first (the
+// common case, where the phase completed already), then the bounded slow path.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, ctl, site);
 }
 
 // Wait that ignores the abort flag (for draining copies this thread issued itself), still bounded.
