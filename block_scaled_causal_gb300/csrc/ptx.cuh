@@ -60,10 +60,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Slow path of mbar_wait: bounded by the wall clock.  Returns false if another thread of the CTA
-// has aborted, or if this wait ran past the limit (then it records `site` in the device status
-// word and raises the CTA's abort flag).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
+// Bounded wait for the phase with `parity` of an mbarrier, fully inline (a call would make the
+// caller save its live registers).  An inline non-blocking test first (the common case, where the
+// phase completed already), then try_wait in a loop bounded by the wall clock.  Returns false if
+// another thread of the CTA has aborted, or if this wait ran past the limit (then it records
+// `site` in the device status word and raises the CTA's abort flag).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -78,15 +81,8 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
-// Bounded wait for the phase with `parity` of an mbarrier: an inline non-blocking test first (the
-// common case, where the phase completed already), then the bounded slow path.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
-  if (mbar_test_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, ctl, site);
-}
-
 // Wait that ignores the abort flag (for draining copies this thread issued itself), still bounded.
-static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > limit_ns) return false;
