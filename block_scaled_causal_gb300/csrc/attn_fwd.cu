@@ -15,9 +15,9 @@
 //               through a 4-stage ring; the own-block token-normalised V tile once.
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.cp (scale factors) and tcgen05.mma.
 //   warps 2-3   decode the token-normalised V tile to BF16 (exact) in the MMA operand layout.
-//   warps 4-11  softmax: two warpgroups, each owning one 64-column half of every S row (warps 4+q
-//               and 8+q share TMEM lane quarter q = query rows 32q..32q+31); the row maximum is
-//               exchanged through shared memory once per key tile.  Then the epilogue.
+//   warps 4-11  softmax: each warp owns 16 query rows (TMEM 16x256b shape: a row's keys spread over
+//               a quad of lanes, reductions are quad shuffles); then the epilogue, where warps 4+q
+//               and 8+q store the two 64-column halves of rows 32q..32q+31.
 // TMEM (512 columns): S[0] 0-127, S[1] 128-255, O 256-383, scale factors from 384.
 // P (E4M3, 32 columns per term) is written over the S buffer it came from; the own-block BF16 P
 // goes to the other S buffer.
@@ -52,7 +52,7 @@ constexpr uint32_t OFF_SFV = OFF_SFK + NST * 512;        // NST stages
 constexpr uint32_t OFF_SFP = OFF_SFV + NST * 512;        // P scale blocks: term 0, term 1
 constexpr uint32_t OFF_VTNSC = OFF_SFP + 2 * 512;        // 128 token amplitudes
 constexpr uint32_t OFF_RED = OFF_VTNSC + 128;            // float [2 parity][2 halves][128 rows] maxima
-constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4; // float [2 halves][128 rows] row sums
+constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4; // float [l | m][128 rows]
 constexpr uint32_t OFF_BAR = OFF_REDL + 2 * 128 * 4;
 constexpr uint32_t NUM_BARS = 32;
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;    // tmem slot, abort flag
@@ -271,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int k0 = kc * 8 + 2 * e;
+              // slots 8kc + 2e + {0,1} carry keys k0, k0 + 1 (the order of the own-block BF16 P)
+              const int k0 = 16 * (kc >> 1) + 8 * (e & 1) + 4 * (kc & 1) + 2 * (e >> 1);
               const uint16_t pair = (uint16_t)raw[k0 * HD + d] | ((uint16_t)raw[(k0 + 1) * HD + d] << 8);
               const uint32_t h2 = cvt_e4m3x2_to_f16x2(pair);
               const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * pow2_e8m0(amp[k0]);
@@ -287,127 +288,145 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_arrive(bar(B_VT_READY));
     }
   } else {
-    // ======================= softmax + epilogue (256 threads: row r, column half h)
-    const int q = warp & 3;             // TMEM lane quarter == 32-row query sub-block of the tile
-    const int h = (warp - 4) >> 2;      // column half: keys / O columns [64h, 64h + 64)
-    const int r = q * 32 + lane;        // row inside the tile
-    const int i = t * BM + r;           // query token
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    // ======================= softmax + epilogue (256 threads)
+    // Warp w (4..11) owns the 16 query rows 32q + 16hf .. +15 of the tile (q = w % 4 is its TMEM
+    // lane quarter, hf = (w - 4) / 4).  With the 16x256b TMEM shape, thread t holds rows
+    // ra = base + t/4 and rb = ra + 8 for the keys 8k + 2(t%4) + {0,1}, k = 0..15: a row's 128
+    // keys are spread over the four threads of a quad, so row reductions are quad shuffles and the
+    // eight softmax warps run independently.  P is written in the same layout; inside each 32-key
+    // block the MMA's K slot 8a + 2b + e carries key 8b + 2a + e (a 4x4 transpose of key pairs),
+    // and the columnwise V bytes are stored in that key order, so P.V sums the same products.
+    const int q = warp & 3;
+    const int hf = (warp - 4) >> 2;
+    const int qd = lane & 3;
+    const int base = q * 32 + hf * 16;
+    const int ra = base + (lane >> 2), rb = ra + 8;    // rows inside the tile
+    const uint32_t lane_off = (uint32_t)base << 16;
     const float sl2 = a.scale_log2e;
-    float* red = reinterpret_cast<float*>(smem + OFF_RED);     // [parity][half][row]
-    float* redl = reinterpret_cast<float*>(smem + OFF_REDL);   // [half][row]
-    // Exponentials are taken against m_used, a running row maximum (log2 units) that is raised only
-    // when a tile's maximum exceeds it by more than RESCALE_LOG2; O and l are rescaled then.  The
-    // weights p' = 2^(x - m_used + P_SHIFT) stay below 2^(P_SHIFT + RESCALE_LOG2) < 448, inside the
-    // E4M3 range, and every decision depends only on this row's visible scores.
-    float m_used = -INFINITY;
-    float2 lacc[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) lacc[g] = make_float2(0.f, 0.f);
+    float* redl = reinterpret_cast<float*>(smem + OFF_REDL);   // [l | m][128 rows]
+    // Exponentials are taken against m_a / m_b, running row maxima (log2 units) raised only when a
+    // tile's maximum exceeds them by more than RESCALE_LOG2; O is rescaled then.  The weights
+    // p' = 2^(x - m + P_SHIFT) stay below 2^(P_SHIFT + RESCALE_LOG2) < 448, inside the E4M3 range,
+    // and every decision depends only on the row's own visible scores.
+    float m_a = -INFINITY, m_b = -INFINITY;
+    float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);   // partial row sums (this quad lane)
     bool ok = true;
-#define SV(c) s[(c) >> 5][(c) & 31]
     for (int j = 0; j <= t; ++j) {
       const int sb = j & 1;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, ctl, W_SM_S));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tSb = tmem + (sb ? T_S1 : T_S0) + lane_off;
-      float s[2][32];   // this thread's 64 scores: keys 64h + c
-      tmem_ld32f(tSb + 64 * h, s[0]);
-      tmem_ld32f(tSb + 64 * h + 32, s[1]);
+      float v[64];
+      tmem_ld16x256_x16(tSb, v);
       tmem_ld_wait();
       const bool diag = (j == t);
       if (diag) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) SV(c) = (64 * h + c > r) ? -INFINITY : SV(c);
-      }
-      // partial row maximum of the raw scores in 4 independent chains, exchanged with the partner
-      float mx[4];
+        for (int k = 0; k < 16; ++k) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int c0 = 16 * g;
-        float v = fmax3(SV(c0), SV(c0 + 1), SV(c0 + 2));
-#pragma unroll
-        for (int k = 3; k < 15; k += 2) v = fmax3(v, SV(c0 + k), SV(c0 + k + 1));
-        mx[g] = fmaxf(v, SV(c0 + 15));
+          for (int e = 0; e < 2; ++e) {
+            const int key = 8 * k + 2 * qd + e;
+            v[4 * k + e] = key > ra ? -INFINITY : v[4 * k + e];
+            v[4 * k + 2 + e] = key > rb ? -INFINITY : v[4 * k + 2 + e];
+          }
+        }
       }
-      const float pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      red[(sb * 2 + h) * 128 + r] = pm;
-      pair_sync(q);
-      const float mt = fmaxf(red[(sb * 2 + 0) * 128 + r], red[(sb * 2 + 1) * 128 + r]) * sl2;
-      const bool need = mt > m_used + RESCALE_LOG2;      // always true at the first tile
-      const float m_new = need ? mt : m_used;
-      const bool resc = need && (j > 0);
+      // row maxima: 32 values per row in this lane (k = 0..15), then across the quad
+      float xa0 = fmax3(v[0], v[1], v[4]), xa1 = fmax3(v[5], v[8], v[9]);
+      float xb0 = fmax3(v[2], v[3], v[6]), xb1 = fmax3(v[7], v[10], v[11]);
+#pragma unroll
+      for (int k = 3; k < 15; k += 2) {
+        xa0 = fmax3(xa0, v[4 * k], v[4 * k + 1]);
+        xa1 = fmax3(xa1, v[4 * k + 4], v[4 * k + 5]);
+        xb0 = fmax3(xb0, v[4 * k + 2], v[4 * k + 3]);
+        xb1 = fmax3(xb1, v[4 * k + 6], v[4 * k + 7]);
+      }
+      float mta = fmax3(xa0, xa1, fmaxf(v[60], v[61])), mtb = fmax3(xb0, xb1, fmaxf(v[62], v[63]));
+      mta = fmaxf(mta, __shfl_xor_sync(0xFFFFFFFFu, mta, 1));
+      mtb = fmaxf(mtb, __shfl_xor_sync(0xFFFFFFFFu, mtb, 1));
+      mta = fmaxf(mta, __shfl_xor_sync(0xFFFFFFFFu, mta, 2)) * sl2;
+      mtb = fmaxf(mtb, __shfl_xor_sync(0xFFFFFFFFu, mtb, 2)) * sl2;
+      const bool need_a = mta > m_a + RESCALE_LOG2, need_b = mtb > m_b + RESCALE_LOG2;   // true at j = 0
+      const float mna = need_a ? mta : m_a, mnb = need_b ? mtb : m_b;
+      const bool resc = (need_a || need_b) && (j > 0);
       bool pv_waited = false;
       if (__any_sync(0xFFFFFFFFu, resc)) {
-        // rescale this thread's half of its O row (factor 1 where the row keeps its max): needs
-        // PV_{j-1} done
+        // rescale this warp's O rows (factor 1 for rows that keep their max): needs PV_{j-1} done
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_FREE + (j - 1) % NST), ((j - 1) / NST) & 1, ctl, W_SM_PV));
         if (!ok) break;
         pv_waited = true;
         tc_fence_after();
-        const float alpha = resc ? ex2_approx(m_used - m_new) : 1.0f;
-        const uint32_t tOb = tmem + T_O + lane_off + 64 * h;
-        float o0[32], o1[32];
-        tmem_ld32f(tOb, o0);
-        tmem_ld32f(tOb + 32, o1);
+        const float alpha_a = (need_a && j > 0) ? ex2_approx(m_a - mna) : 1.0f;
+        const float alpha_b = (need_b && j > 0) ? ex2_approx(m_b - mnb) : 1.0f;
+        const uint32_t tOb = tmem + T_O + lane_off;
+        uint32_t o[64];
+        tmem_ld16x256_x16u(tOb, o);
         tmem_ld_wait();
-        uint32_t u0[32], u1[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          u0[k] = __float_as_uint(o0[k] * alpha);
-          u1[k] = __float_as_uint(o1[k] * alpha);
+        for (int k = 0; k < 16; ++k) {
+          o[4 * k + 0] = __float_as_uint(__uint_as_float(o[4 * k + 0]) * alpha_a);
+          o[4 * k + 1] = __float_as_uint(__uint_as_float(o[4 * k + 1]) * alpha_a);
+          o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * alpha_b);
+          o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * alpha_b);
         }
-        tmem_st32(tOb, u0);
-        tmem_st32(tOb + 32, u1);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          lacc[g].x *= alpha;
-          lacc[g].y *= alpha;
-        }
+        tmem_st16x256_x16(tOb, o);
+        la.x *= alpha_a; la.y *= alpha_a;
+        lb.x *= alpha_b; lb.y *= alpha_b;
       }
-      m_used = m_new;
-      // p' = 2^(s * scale*log2(e) - m_used + P_SHIFT), two lanes per packed FMA
+      m_a = mna;
+      m_b = mnb;
+      // p' = 2^(s * scale*log2(e) - m + P_SHIFT)
       const float2 mul2 = make_float2(sl2, sl2);
-      const float2 add2 = make_float2(P_SHIFT - m_used, P_SHIFT - m_used);
+      const float2 adda = make_float2(P_SHIFT - m_a, P_SHIFT - m_a), addb = make_float2(P_SHIFT - m_b, P_SHIFT - m_b);
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float2 x2 = __ffma2_rn(make_float2(SV(c), SV(c + 1)), mul2, add2);
-        SV(c) = ex2_approx(x2.x);
-        SV(c + 1) = ex2_approx(x2.y);
-        lacc[(c >> 1) & 3] = __fadd2_rn(lacc[(c >> 1) & 3], make_float2(SV(c), SV(c + 1)));
+      for (int k = 0; k < 16; ++k) {
+        const float2 xa = __ffma2_rn(make_float2(v[4 * k], v[4 * k + 1]), mul2, adda);
+        const float2 xb = __ffma2_rn(make_float2(v[4 * k + 2], v[4 * k + 3]), mul2, addb);
+        v[4 * k] = ex2_approx(xa.x);
+        v[4 * k + 1] = ex2_approx(xa.y);
+        v[4 * k + 2] = ex2_approx(xb.x);
+        v[4 * k + 3] = ex2_approx(xb.y);
+        la = __fadd2_rn(la, make_float2(v[4 * k], v[4 * k + 1]));
+        lb = __fadd2_rn(lb, make_float2(v[4 * k + 2], v[4 * k + 3]));
       }
-      // E4M3 P for completed keys (scale 2^-P_SHIFT; a second term holds the residual at 2^-4 of
-      // that); in the diagonal tile the own and later 32-key blocks are 0 (the leaky control keeps
-      // the own block on this path instead).  Key block kb = 2h + kk of the tile.
+      // E4M3 P (scale 2^-P_SHIFT; a second term holds the residual at 2^-4 of that) over this S
+      // buffer: block kb's columns 8kb + 2qd and 8kb + 2qd + 1 carry keys {8(4kb) + 2qd + e,
+      // 8(4kb+1) + 2qd + e} and {8(4kb+2) ..., 8(4kb+3) ...}.  In the diagonal tile the own and later
+      // 32-key blocks are 0 (the leaky control keeps the own block on this path instead).
       const int fp8_limit = diag ? (LEAKY ? q + 1 : q) : 4;
+      uint32_t w0[16], w1[16];
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int kb = 2 * h + kk;
+      for (int kb = 0; kb < 4; ++kb) {
         const bool use = kb < fp8_limit;
-        uint32_t w0[8], w1[8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int c = kk * 32 + g * 4;
-          const float p0 = use ? SV(c) : 0.f, p1 = use ? SV(c + 1) : 0.f;
-          const float p2 = use ? SV(c + 2) : 0.f, p3 = use ? SV(c + 3) : 0.f;
-          const uint16_t h01 = cvt_e4m3x2(p0, p1), h23 = cvt_e4m3x2(p2, p3);
-          w0[g] = (uint32_t)h01 | ((uint32_t)h23 << 16);
-          if (P_TERMS > 1) {
-            const uint32_t f01 = cvt_e4m3x2_to_f16x2(h01), f23 = cvt_e4m3x2_to_f16x2(h23);
-            const float d0 = p0 - __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFFu)));
-            const float d1 = p1 - __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
-            const float d2 = p2 - __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFFu)));
-            const float d3 = p3 - __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
-            w1[g] = (uint32_t)cvt_e4m3x2(d0 * 16.f, d1 * 16.f) | ((uint32_t)cvt_e4m3x2(d2 * 16.f, d3 * 16.f) << 16);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int k0 = 4 * kb + 2 * c2;   // keys 8k0 + 2qd + e and 8(k0+1) + 2qd + e
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const float p0 = use ? v[4 * k0 + 2 * rr] : 0.f, p1 = use ? v[4 * k0 + 2 * rr + 1] : 0.f;
+            const float p2 = use ? v[4 * k0 + 4 + 2 * rr] : 0.f, p3 = use ? v[4 * k0 + 4 + 2 * rr + 1] : 0.f;
+            const uint16_t h01 = cvt_e4m3x2(p0, p1), h23 = cvt_e4m3x2(p2, p3);
+            w0[4 * kb + 2 * rr + c2] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+            if (P_TERMS > 1) {
+              const uint32_t f01 = cvt_e4m3x2_to_f16x2(h01), f23 = cvt_e4m3x2_to_f16x2(h23);
+              const float d0 = p0 - __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFFu)));
+              const float d1 = p1 - __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
+              const float d2 = p2 - __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFFu)));
+              const float d3 = p3 - __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
+              w1[4 * kb + 2 * rr + c2] =
+                  (uint32_t)cvt_e4m3x2(d0 * 16.f, d1 * 16.f) | ((uint32_t)cvt_e4m3x2(d2 * 16.f, d3 * 16.f) << 16);
+            }
           }
         }
-        tmem_st8(tSb + kb * 8, w0);
-        if (P_TERMS > 1) tmem_st8(tSb + 32 + kb * 8, w1);
       }
+      tmem_st16x256_x4(tSb, w0);
+      if (P_TERMS > 1) tmem_st16x256_x4(tSb + 32, w1);
       if (diag && !LEAKY) {
-        // own block (keys of sub-block q, j <= i) as BF16 P (P_TERMS terms) into the other S
-        // buffer, which PV_{t-1} may still be reading
+        // own block (keys of sub-block q, key <= row) as BF16 P (P_TERMS terms) into the other S
+        // buffer once PV_{t-1}, its last reader, is done.  16-key group g16: column 8g16 + 2qd
+        // carries keys 16g16 + 2qd + e, column 8g16 + 2qd + 1 keys 16g16 + 8 + 2qd + e (the decoded
+        // V tile uses the same key order).
         if (t > 0 && !pv_waited) {
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_FREE + (t - 1) % NST), ((t - 1) / NST) & 1, ctl, W_SM_PV));
           if (!ok) break;
@@ -415,57 +434,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         const uint32_t tPo = tmem + (sb ? T_S0 : T_S1) + lane_off;
         const float unshift = 1.0f / (float)(1 << (int)P_SHIFT);
+        uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const int kb = 2 * h + kk;
-          uint32_t hi[16], lo[16];
+        for (int g16 = 0; g16 < 8; ++g16) {
+          const bool own = (g16 >> 1) == q;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = kk * 32 + 2 * e;
-            const float p0 = (kb == q) ? SV(c) * unshift : 0.f;
-            const float p1 = (kb == q) ? SV(c + 1) * unshift : 0.f;
-            hi[e] = pack_bf16x2(p0, p1);
-            lo[e] = pack_bf16x2(p0 - __uint_as_float(hi[e] << 16), p1 - __uint_as_float(hi[e] & 0xFFFF0000u));
+          for (int m = 0; m < 2; ++m) {
+            const int k = 2 * g16 + m;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const float p0 = own ? v[4 * k + 2 * rr] * unshift : 0.f;
+              const float p1 = own ? v[4 * k + 2 * rr + 1] * unshift : 0.f;
+              const uint32_t hh = pack_bf16x2(p0, p1);
+              hi[4 * g16 + 2 * rr + m] = hh;
+              lo[4 * g16 + 2 * rr + m] =
+                  pack_bf16x2(p0 - __uint_as_float(hh << 16), p1 - __uint_as_float(hh & 0xFFFF0000u));
+            }
           }
-          tmem_st16(tPo + kb * 16, hi);
-          if (P_TERMS > 1) tmem_st16(tPo + 64 + kb * 16, lo);
         }
+        tmem_st16x256_x8(tPo, hi);
+        if (P_TERMS > 1) tmem_st16x256_x8(tPo + 64, lo);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL + sb));
     }
-#undef SV
-    // ---- epilogue: O / l -> BF16 (this thread's 64 columns), LSE (natural log)
-    redl[h * 128 + r] = ((lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y)) +
-                        ((lacc[2].x + lacc[2].y) + (lacc[3].x + lacc[3].y));
+    // ---- epilogue: row sums across the quad, then O / l -> BF16 and the LSE, with the 32x32b
+    // shape: warp 4+q stores columns 0-63 and warp 8+q columns 64-127 of rows 32q..32q+31
+    float sa = la.x + la.y, sbm = lb.x + lb.y;
+    sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 1);
+    sbm += __shfl_xor_sync(0xFFFFFFFFu, sbm, 1);
+    sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 2);
+    sbm += __shfl_xor_sync(0xFFFFFFFFu, sbm, 2);
+    if (qd == 0) {
+      redl[ra] = sa;
+      redl[rb] = sbm;
+      redl[128 + ra] = m_a;
+      redl[128 + rb] = m_b;
+    }
     pair_sync(q);
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_O_FULL), 0, ctl, W_SM_O));
     if (ok) {
       tc_fence_after();
-      const float l = redl[r] + redl[128 + r];
+      const int h = hf;
+      const int r = q * 32 + lane;        // row inside the tile
+      const int i = t * BM + r;           // query token
+      const float l = redl[r], m_fin = redl[128 + r];
       const float inv_l = (float)(1 << (int)P_SHIFT) / l;
       const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq
                                           : ((long long)i * a.B + b) * a.Hq + hq;
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + row * HD + 64 * h);
-      const uint32_t tOb = tmem + T_O + lane_off + 64 * h;
+      const uint32_t tOb = tmem + T_O + ((uint32_t)(q * 32) << 16) + 64 * h;
       float o[2][32];
       tmem_ld32f(tOb, o[0]);
       tmem_ld32f(tOb + 32, o[1]);
       tmem_ld_wait();
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
+      for (int e8 = 0; e8 < 8; ++e8) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int k = g * 8 + 2 * e;
+          const int k = e8 * 8 + 2 * e;
           w[e] = pack_bf16x2(o[k >> 5][k & 31] * inv_l, o[(k + 1) >> 5][(k + 1) & 31] * inv_l);
         }
-        orow[g] = make_uint4(w[0], w[1], w[2], w[3]);
+        orow[e8] = make_uint4(w[0], w[1], w[2], w[3]);
       }
       if (h == 0) {
         const float ln2 = 0.69314718055994531f;
-        a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m_used + lg2_approx(l) - P_SHIFT) * ln2;
+        a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m_fin + lg2_approx(l) - P_SHIFT) * ln2;
       }
     }
   }

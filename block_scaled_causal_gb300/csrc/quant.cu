@@ -87,7 +87,9 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint4* __restr
 
 // ------------------------------------------------------------------------------------------
 // V quantiser: one CTA per (b, h, 128-token tile), 256 threads.  Produces either or both of
-//   * the columnwise copy, transposed: vt[((b*H + h)*D + d)*S + s], with scale atoms
+//   * the columnwise copy, transposed, with the tokens of each aligned 32-token block in the order
+//     perm32 (the order the attention kernel's P operand uses, see bsc.h):
+//     vt[((b*H + h)*D + d)*S + 32*blk + x] = token 32*blk + perm32(x), with scale atoms
 //       vsc[((b*H + h)*(S/128) + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32];
 //   * the token-normalised copy in V's own layout with scales vtn_sc[(b*H + h)*S + s].
 constexpr int VQ_ROWS = 128;
@@ -143,13 +145,16 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
   float inv0, inv1;
   const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0);
   const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1);
+  // Byte slot s of the 32-token block holds token perm32(s) = 8*((s%8)/2) + 2*(s/8) + s%2: word i
+  // (slots 4i..4i+3) holds tokens k0, k0+1, k0+8, k0+9 with k0 = 16*(i%2) + 2*(i/2).
   uint32_t o0[8], o1[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint32_t lo0 = cvt_e4m3x2(bf16_lo(w[4 * i]) * inv0, bf16_lo(w[4 * i + 1]) * inv0);
-    uint32_t hi0 = cvt_e4m3x2(bf16_lo(w[4 * i + 2]) * inv0, bf16_lo(w[4 * i + 3]) * inv0);
-    uint32_t lo1 = cvt_e4m3x2(bf16_hi(w[4 * i]) * inv1, bf16_hi(w[4 * i + 1]) * inv1);
-    uint32_t hi1 = cvt_e4m3x2(bf16_hi(w[4 * i + 2]) * inv1, bf16_hi(w[4 * i + 3]) * inv1);
+    const int k0 = 16 * (i & 1) + 2 * (i >> 1);
+    uint32_t lo0 = cvt_e4m3x2(bf16_lo(w[k0]) * inv0, bf16_lo(w[k0 + 1]) * inv0);
+    uint32_t hi0 = cvt_e4m3x2(bf16_lo(w[k0 + 8]) * inv0, bf16_lo(w[k0 + 9]) * inv0);
+    uint32_t lo1 = cvt_e4m3x2(bf16_hi(w[k0]) * inv1, bf16_hi(w[k0 + 1]) * inv1);
+    uint32_t hi1 = cvt_e4m3x2(bf16_hi(w[k0 + 8]) * inv1, bf16_hi(w[k0 + 9]) * inv1);
     o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu : (lo0 | (hi0 << 16));
     o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
   }

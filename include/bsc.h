@@ -25,7 +25,12 @@
  * Data layouts (BSHD: [B][S][H][D]; SBHD: [S][B][H][D]; D fastest in both):
  *   x_bf16, v_bf16, o_bf16    bf16 in the given layout
  *   x_e4m3, vtn_e4m3          E4M3 bytes, same layout and strides as the bf16 input
- *   v_e4m3_t                  E4M3 bytes of V transposed: [B][H][D][S]
+ *   v_e4m3_t                  E4M3 bytes of V transposed, [B][H][D][S], with the tokens of each
+ *                             aligned 32-token block in the order the attention kernel's P operand
+ *                             uses: byte 32*blk + x holds token 32*blk + perm32(x), where
+ *                             perm32(x) = 8*((x%8)/2) + 2*(x/8) + x%2 (a 4x4 transpose of token
+ *                             pairs; perm32(perm32(x)) = x).  Scales are unaffected: a block keeps
+ *                             its 32 tokens.
  *   Scale bytes are E8M0 (value 2^(byte-127); 0xFF = NaN) and come in two forms:
  *   "row atoms" (Q and K rowwise scales):  one byte per (b, h, s, c) with c = d/32, at
  *        ((b*H + h)*(S/128) + s/128)*512 + (s%32)*16 + ((s%128)/32)*4 + c
@@ -84,7 +89,8 @@ bsc_status mxfp8_quantize_qk_rowwise(const void* x_bf16, int B, int S, int H, in
 /*
  * Columnwise MXFP8 quantisation of V: one E8M0 scale per 32 consecutive tokens of each (b, h, d)
  * ("A columnwise MXFP8 V scale is shared by 32 consecutive tokens", PR #3865 Description).
- *   v_bf16 [in] bf16 in `layout`;  v_e4m3_t [out] [B][H][D][S];  v_sc [out] column atoms,
+ *   v_bf16 [in] bf16 in `layout`;  v_e4m3_t [out] [B][H][D][S] (perm32 order within 32-token
+ *   blocks);  v_sc [out] column atoms,
  *   B*H*(S/32)*D bytes.
  */
 bsc_status mxfp8_quantize_v_colwise(const void* v_bf16, int B, int S, int H, int D, bsc_layout layout,
@@ -109,7 +115,7 @@ typedef struct {
   const uint8_t* q_sc;    /* [in] Q row atoms */
   const uint8_t* k;       /* [in] K E4M3 bytes, `layout`, Hkv heads */
   const uint8_t* k_sc;    /* [in] K row atoms */
-  const uint8_t* v_t;     /* [in] V columnwise E4M3 bytes, [B][Hkv][D][S] */
+  const uint8_t* v_t;     /* [in] V columnwise E4M3 bytes, [B][Hkv][D][S], perm32 order */
   const uint8_t* v_sc;    /* [in] V column atoms */
   const uint8_t* vtn;     /* [in] token-normalised V bytes, `layout` (unused when leaky = 1) */
   const uint8_t* vtn_sc;  /* [in] token amplitudes [B][Hkv][S] (unused when leaky = 1) */

@@ -20,6 +20,20 @@ def col_atoms_to_compact(atoms: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(a.transpose(0, 1, 4, 3, 2, 5)).reshape(B, H, 128, T * 4)
 
 
+def perm32():
+    """Token order inside each 32-token block of the columnwise V bytes: byte x holds token
+    8*((x%8)//2) + 2*(x//8) + x%2 (an involution)."""
+    x = np.arange(32)
+    return 8 * ((x % 8) // 2) + 2 * (x // 8) + x % 2
+
+
+def vt_to_token_order(vt: np.ndarray) -> np.ndarray:
+    """[.., S] columnwise V bytes in perm32 order -> token order."""
+    S = vt.shape[-1]
+    blocks = vt.reshape(vt.shape[:-1] + (S // 32, 32))
+    return np.ascontiguousarray(blocks[..., perm32()]).reshape(vt.shape)
+
+
 def bshd_np(x: torch.Tensor, layout: int) -> np.ndarray:
     """CPU numpy copy of a tensor stored in `layout`, viewed as [B,S,H,D]."""
     t = I.to_bshd(x.cpu(), layout)

@@ -104,3 +104,13 @@ def test_attn_validation(ops, kw, want):
 def test_attn_null_params(ops):
     assert ops.lib.mxfp8_causal_attn_fwd(None, None) == 1
     assert ops.lib.bsc_read_device_status(None, None) == 1
+
+
+def test_perm32_is_an_involution_within_blocks():
+    import numpy as np
+    from tests._helpers import perm32, vt_to_token_order
+    p = perm32()
+    assert sorted(p) == list(range(32)) and (p[p] == np.arange(32)).all()
+    x = np.arange(64, dtype=np.int64)[None]
+    y = vt_to_token_order(x)
+    assert (y[0, :32] == p).all() and (y[0, 32:] == 32 + p).all()

@@ -7,7 +7,7 @@ import torch
 
 from block_scaled_causal_gb300 import inputs as I
 from oracle import mx
-from tests._helpers import bshd_np, col_atoms_to_compact, row_atoms_to_compact
+from tests._helpers import bshd_np, col_atoms_to_compact, row_atoms_to_compact, vt_to_token_order
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +39,7 @@ def _check_v(ops, v_cpu, layout, tokens=None):
     for a, b in ((vt, vt2), (vsc, vsc2), (vtn, vtn2), (vtn_sc, vtn_sc2)):
         assert torch.equal(a, b)
     vb = bshd_np(v_cpu, layout).astype(np.float64)
-    g_vt = vt.cpu().numpy()
+    g_vt = vt_to_token_order(vt.cpu().numpy())
     g_vsc = col_atoms_to_compact(vsc.cpu().numpy())
     g_vtn = bshd_np(vtn, layout)
     g_vtn_sc = vtn_sc.cpu().numpy()
