@@ -165,6 +165,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_arrive_expect_tx(bar(B_Q_FULL), BM * HD + 512);
       tma_load_4d(sbase + OFF_Q, &a.tm_q, bar(B_Q_FULL), 0, hq, t * BM, b);
       bulk_load(sbase + OFF_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + t) * 512, 512, bar(B_Q_FULL));
+      if (own_split) {
+        // the own-block tile of the token-normalised V, decoded early by warps 2-3
+        prefetch_tensormap(&a.tm_vtn);
+        mbar_arrive_expect_tx(bar(B_VTN_FULL), BN * HD + BN);
+        tma_load_4d(sbase + OFF_VTN8, &a.tm_vtn, bar(B_VTN_FULL), 0, hk, t * BN, b);
+        bulk_load(sbase + OFF_VTNSC, a.vtn_sc + kv_plane * a.S + (long long)t * BN, BN, bar(B_VTN_FULL));
+      }
       int nl[NST] = {};   // stage loads issued
       bool ok = true;
       for (int j = 0; j <= t && ok; ++j) {
@@ -177,25 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         bulk_load(sbase + OFF_SFV + st * 512, a.v_sc + (kv_plane * T + j) * 512, 512, bar(B_FULL + st));
         ++nl[st];
       }
-      bool vtn_issued = false;
-      if (own_split && ok) {
-        prefetch_tensormap(&a.tm_vtn);
-        mbar_arrive_expect_tx(bar(B_VTN_FULL), BN * HD + BN);
-        tma_load_4d(sbase + OFF_VTN8, &a.tm_vtn, bar(B_VTN_FULL), 0, hk, t * BN, b);
-        bulk_load(sbase + OFF_VTNSC, a.vtn_sc + kv_plane * a.S + (long long)t * BN, BN, bar(B_VTN_FULL));
-        vtn_issued = true;
-      }
       // drain: every copy this thread issued must land before the CTA may exit
       for (int st = 0; st < NST; ++st) {
         if (nl[st] > 0) mbar_wait_drain(bar(B_FULL + st), (nl[st] - 1) & 1, a.limit_ns);
       }
       mbar_wait_drain(bar(B_Q_FULL), 0, a.limit_ns);
-      if (vtn_issued) mbar_wait_drain(bar(B_VTN_FULL), 0, a.limit_ns);
+      if (own_split) mbar_wait_drain(bar(B_VTN_FULL), 0, a.limit_ns);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer
     if (lane == 0) {
       const uint32_t tS[2] = {tmem + T_S0, tmem + T_S1};
+      const uint64_t dQ = desc_kmajor_sw128(sbase + OFF_Q), dK = desc_kmajor_sw128(sbase + OFF_K),
+                     dV = desc_kmajor_sw128(sbase + OFF_V);   // descriptors: start address in 16-byte units
+      const uint64_t dSFK = desc_sf_block(sbase + OFF_SFK), dSFV = desc_sf_block(sbase + OFF_SFV);
       const uint32_t tO = tmem + T_O;
       bool ok = true;
       if (a.inject_stall) ok = mbar_wait(bar(B_INJECT), 0, ctl, W_MMA_INJECT);   // nothing arrives here
@@ -214,12 +216,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int j = jj, st = j % NST, sb = j & 1;
           if (!(ok = mbar_wait(bar(B_FULL + st), (j / NST) & 1, ctl, W_MMA_KV))) break;
           tc_fence_after();
-          tc_cp_32x128b_warpx4(tmem + T_SFK + 4 * sb, desc_sf_block(sbase + OFF_SFK + st * 512));
-          tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * sb, desc_sf_block(sbase + OFF_SFV + st * 512));
+          tc_cp_32x128b_warpx4(tmem + T_SFK + 4 * sb, dSFK + (uint64_t)(st * 32));
+          tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * sb, dSFV + (uint64_t)(st * 32));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8_ss(tS[sb], desc_kmajor_sw128(sbase + OFF_Q + kk * 32),
-                        desc_kmajor_sw128(sbase + OFF_K + st * BN * HD + kk * 32), idesc_mxf8(BM, BN, kk, kk),
+            mma_mxf8_ss(tS[sb], dQ + 2 * kk,
+                        dK + (uint64_t)(st * (BN * HD / 16) + 2 * kk), idesc_mxf8(BM, BN, kk, kk),
                         tmem + T_SFQ, tmem + T_SFK + 4 * sb, kk > 0 ? 1u : 0u);
           }
           tc_commit(bar(B_S_FULL + sb));
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               mma_mxf8_ts(tO, tS[sb] + term * 32 + kk * 8,
-                          desc_kmajor_sw128(sbase + OFF_V + st * HD * BN + kk * 32), idesc_mxf8(BM, HD, kk, kk),
+                          dV + (uint64_t)(st * (HD * BN / 16) + 2 * kk), idesc_mxf8(BM, HD, kk, kk),
                           tmem + T_SFP + 4 * term, tmem + T_SFV + 4 * sb, (j > 0 || term > 0 || kk > 0) ? 1u : 0u);
             }
           }
