@@ -67,8 +67,7 @@ enum Bar : uint32_t {
   B_FULL = 1,                    // + stage
   B_FREE = B_FULL + NST,         // + stage
   B_S_FULL = B_FREE + NST,       // + S buffer
-  B_P_FULL = B_S_FULL + 2,       // + S buffer
-  B_O_FULL = B_P_FULL + 2,
+  B_O_FULL = B_S_FULL + 2,
   B_VTN_FULL,
   B_VT_READY,
   B_DRAIN,
@@ -90,7 +89,7 @@ constexpr uint8_t SFP_TERM1 = 127 - 12;
 
 // wait-site codes reported through the device status word
 enum Site : int {
-  W_PROD_FREE = 1, W_MMA_Q, W_MMA_KV, W_MMA_P, W_MMA_VT, W_MMA_INJECT,
+  W_PROD_FREE = 1, W_MMA_Q, W_FWD_KV, W_MMA_VT, W_MMA_INJECT,
   W_SM_S, W_SM_PV, W_SM_O, W_DEC_VTN,
 };
 
@@ -99,6 +98,16 @@ __device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
 }
 
 // Named barrier for the two softmax warps that share a TMEM lane quarter.
+// Hardware named barriers between the MMA warp and the warps it waits for.  Unlike an mbarrier
+// wait, which returns only once the waiting thread's tcgen05 MMAs in flight have drained, a named
+// barrier leaves the tensor pipe busy.  Every participant passes every generation of these
+// barriers, also after an abort, so none of them can wait forever.
+constexpr uint32_t NB_KV = 5;   // forwarder warp + MMA warp: K_j, V_j landed
+constexpr uint32_t NB_P = 6;    // softmax warps + MMA warp: P_j written
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void pair_sync(int q) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
 }
@@ -130,11 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_P_FULL + s), kSoftmaxThreads);
     }
     mbar_init(bar(B_O_FULL), 1);
     mbar_init(bar(B_VTN_FULL), 1);
-    mbar_init(bar(B_VT_READY), 64);
+    mbar_init(bar(B_VT_READY), 32);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_INJECT), 1);
     *abort_flag = 0;
@@ -192,14 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (own_split) mbar_wait_drain(bar(B_VTN_FULL), 0, a.limit_ns);
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer
+    // ======================= MMA issuer (lane 0; the whole warp meets the named barriers)
+    const uint32_t tS[2] = {tmem + T_S0, tmem + T_S1};
+    const uint64_t dQ = desc_kmajor_sw128(sbase + OFF_Q), dK = desc_kmajor_sw128(sbase + OFF_K),
+                   dV = desc_kmajor_sw128(sbase + OFF_V);   // descriptors: start address in 16-byte units
+    const uint64_t dSFK = desc_sf_block(sbase + OFF_SFK), dSFV = desc_sf_block(sbase + OFF_SFV);
+    const uint32_t tO = tmem + T_O;
+    bool ok = true;
     if (lane == 0) {
-      const uint32_t tS[2] = {tmem + T_S0, tmem + T_S1};
-      const uint64_t dQ = desc_kmajor_sw128(sbase + OFF_Q), dK = desc_kmajor_sw128(sbase + OFF_K),
-                     dV = desc_kmajor_sw128(sbase + OFF_V);   // descriptors: start address in 16-byte units
-      const uint64_t dSFK = desc_sf_block(sbase + OFF_SFK), dSFV = desc_sf_block(sbase + OFF_SFV);
-      const uint32_t tO = tmem + T_O;
-      bool ok = true;
       if (a.inject_stall) ok = mbar_wait(bar(B_INJECT), 0, ctl, W_MMA_INJECT);   // nothing arrives here
       ok = ok && mbar_wait(bar(B_Q_FULL), 0, ctl, W_MMA_Q);
       if (ok) {
@@ -208,13 +216,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_cp_32x128b_warpx4(tmem + T_SFP, desc_sf_block(sbase + OFF_SFP));
         tc_cp_32x128b_warpx4(tmem + T_SFP + 4, desc_sf_block(sbase + OFF_SFP + 512));
       }
-      // Per key tile j: wait for stage j, copy its K and V scale atoms to TMEM, S_j = Q K_j^T;
-      // then O += P_{j-1} V_{j-1} once the softmax has written P_{j-1} (the own block follows in
-      // the diagonal tile).  Everything one thread issues executes in order.
-      for (int jj = 0; jj <= t + 1 && ok; ++jj) {
-        if (jj <= t) {
+    }
+    // Per key tile j: S_j = Q K_j^T once stage j has landed; then O += P_{j-1} V_{j-1} once the
+    // softmax has written P_{j-1} (the own block follows in the diagonal tile).  Everything one
+    // thread issues executes in order, so S_{j+1} overwrites P_{j-1} only after PV_{j-1} read it.
+    for (int jj = 0; jj <= t + 1; ++jj) {
+      if (jj <= t) {
+        named_sync(NB_KV, 64);
+        if (lane == 0 && ok) {
           const int j = jj, st = j % NST, sb = j & 1;
-          if (!(ok = mbar_wait(bar(B_FULL + st), (j / NST) & 1, ctl, W_MMA_KV))) break;
           tc_fence_after();
           tc_cp_32x128b_warpx4(tmem + T_SFK + 4 * sb, dSFK + (uint64_t)(st * 32));
           tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * sb, dSFV + (uint64_t)(st * 32));
@@ -226,49 +236,56 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           tc_commit(bar(B_S_FULL + sb));
         }
-        if (jj >= 1) {
+      }
+      if (jj >= 1) {
+        named_sync(NB_P, 32 + kSoftmaxThreads);
+        if (lane == 0 && ok) {
           const int j = jj - 1, st = j % NST, sb = j & 1;
-          if (!(ok = mbar_wait(bar(B_P_FULL + sb), (j >> 1) & 1, ctl, W_MMA_P))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int term = 0; term < P_TERMS; ++term) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              mma_mxf8_ts(tO, tS[sb] + term * 32 + kk * 8,
-                          dV + (uint64_t)(st * (HD * BN / 16) + 2 * kk), idesc_mxf8(BM, HD, kk, kk),
-                          tmem + T_SFP + 4 * term, tmem + T_SFV + 4 * sb, (j > 0 || term > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          if (j == t && own_split) {
-            if (!(ok = mbar_wait(bar(B_VT_READY), 0, ctl, W_MMA_VT))) break;
+          if (j == t && own_split) ok = mbar_wait(bar(B_VT_READY), 0, ctl, W_MMA_VT);
+          if (ok) {
             tc_fence_after();
 #pragma unroll
             for (int term = 0; term < P_TERMS; ++term) {
 #pragma unroll
-              for (int s = 0; s < 8; ++s) {
-                mma_f16_ts(tO, tS[sb ^ 1] + term * 64 + s * 8,
-                           desc_kmajor_sw128(sbase + OFF_VT + (s >> 2) * (HD * 128) + (s & 3) * 32),
-                           idesc_bf16(BM, HD), 1u);
+              for (int kk = 0; kk < 4; ++kk) {
+                mma_mxf8_ts(tO, tS[sb] + term * 32 + kk * 8,
+                            dV + (uint64_t)(st * (HD * BN / 16) + 2 * kk), idesc_mxf8(BM, HD, kk, kk),
+                            tmem + T_SFP + 4 * term, tmem + T_SFV + 4 * sb, (j > 0 || term > 0 || kk > 0) ? 1u : 0u);
               }
             }
+            if (j == t && own_split) {
+#pragma unroll
+              for (int term = 0; term < P_TERMS; ++term) {
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                  mma_f16_ts(tO, tS[sb ^ 1] + term * 64 + s * 8,
+                             desc_kmajor_sw128(sbase + OFF_VT + (s >> 2) * (HD * 128) + (s & 3) * 32),
+                             idesc_bf16(BM, HD), 1u);
+                }
+              }
+            }
+            tc_commit(bar(B_FREE + st));
           }
-          tc_commit(bar(B_FREE + st));
         }
       }
+      __syncwarp();
+    }
+    if (lane == 0) {
       if (ok) tc_commit(bar(B_O_FULL));
       // drain every tcgen05 operation this thread issued before TMEM is released
       tc_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, a.limit_ns);
     }
-  } else if (warp < 4) {
-    // ======================= own-block V decode (64 threads)
+    __syncwarp();
+  } else if (warp == 2) {
+    // ======================= own-block V decode (32 threads)
     if (own_split) {
-      const int u = threadIdx.x - 64;
+      const int u = lane;
       if (__all_sync(0xFFFFFFFFu, mbar_wait(bar(B_VTN_FULL), 0, ctl, W_DEC_VTN))) {
         const uint8_t* raw = smem + OFF_VTN8;
         const uint8_t* amp = smem + OFF_VTNSC;
-        for (int half = 0; half < 2; ++half) {
-          const int d = u + 64 * half;
+        for (int part = 0; part < 4; ++part) {
+          const int d = u + 32 * part;
           for (int kc = 0; kc < 16; ++kc) {
             uint32_t w[4];
 #pragma unroll
@@ -288,6 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         fence_proxy_async_smem();
       }
       mbar_arrive(bar(B_VT_READY));
+    }
+  } else if (warp == 3) {
+    // ======================= forwarder: stage j has landed -> named barrier with the MMA warp
+    for (int j = 0; j <= t; ++j) {
+      (void)__all_sync(0xFFFFFFFFu, mbar_wait(bar(B_FULL + j % NST), (j / NST) & 1, ctl, W_FWD_KV));
+      named_sync(NB_KV, 64);
     }
   } else {
     // ======================= softmax + epilogue (256 threads)
@@ -315,7 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     bool ok = true;
     for (int j = 0; j <= t; ++j) {
       const int sb = j & 1;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, ctl, W_SM_S));
+      // one pass; a failed wait leaves it early (break) but the tile loop goes on to the barrier
+      do {
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, ctl, W_SM_S));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tSb = tmem + (sb ? T_S1 : T_S0) + lane_off;
@@ -457,9 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_st16x256_x8(tPo, hi);
         if (P_TERMS > 1) tmem_st16x256_x8(tPo + 64, lo);
       }
+      } while (false);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_P_FULL + sb));
+      named_sync(NB_P, 32 + kSoftmaxThreads);   // P_j written (or this warp gave up)
     }
     // ---- epilogue: row sums across the quad, then O / l -> BF16 and the LSE, with the 32x32b
     // shape: warp 4+q stores columns 0-63 and warp 8+q columns 64-127 of rows 32q..32q+31
