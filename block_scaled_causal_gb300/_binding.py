@@ -97,11 +97,11 @@ def _require(x: torch.Tensor, dtype, name):
 
 
 def mxfp8_quantize_qk_rowwise(x, layout=BSHD, out=None, out_sc=None, stream=None):
-    """Returns (E4M3 bytes shaped like x, row-atom scales [B, H, S/128, 512])."""
+    """Returns (E4M3 bytes shaped like x, row-atom scales [B, H, ceil(S/128), 512])."""
     _require(x, torch.bfloat16, "x")
     B, S, H, D = _bshd_dims(x, layout)
     out = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if out is None else out
-    out_sc = torch.empty((B, H, max(S // 128, 0), 512), dtype=torch.uint8, device=x.device) \
+    out_sc = torch.empty((B, H, (S + 127) // 128, 512), dtype=torch.uint8, device=x.device) \
         if out_sc is None else out_sc
     _check(lib.mxfp8_quantize_qk_rowwise(_ptr(x), B, S, H, D, layout, _ptr(out), _ptr(out_sc), _stream(stream)))
     return out, out_sc
@@ -112,7 +112,7 @@ def _v_outputs(v, B, S, H, D, col, tn):
     r = []
     if col:
         r += [torch.empty((B, H, D, S), dtype=torch.uint8, device=dev),
-              torch.empty((B, H, max(S // 128, 0), 512), dtype=torch.uint8, device=dev)]
+              torch.empty((B, H, (S + 127) // 128, 512), dtype=torch.uint8, device=dev)]
     if tn:
         r += [torch.empty(v.shape, dtype=torch.uint8, device=dev),
               torch.empty((B, H, S), dtype=torch.uint8, device=dev)]
@@ -120,7 +120,7 @@ def _v_outputs(v, B, S, H, D, col, tn):
 
 
 def mxfp8_quantize_v_colwise(v, layout=BSHD, stream=None):
-    """Returns (E4M3 bytes of V transposed [B, H, D, S], column-atom scales [B, H, S/128, 512])."""
+    """Returns (E4M3 bytes of V transposed [B, H, D, S], column-atom scales [B, H, ceil(S/128), 512])."""
     _require(v, torch.bfloat16, "v")
     B, S, H, D = _bshd_dims(v, layout)
     vt, vsc = _v_outputs(v, B, S, H, D, True, False)
@@ -180,9 +180,10 @@ def bsc_read_device_status(dev_status, stream=None):
     return lib.bsc_read_device_status(_ptr(dev_status), _stream(stream))
 
 
-def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, stream=None):
+def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, o=None, lse=None, stream=None):
     """The whole hot path on bf16 inputs: quantise Q, K rowwise, V columnwise + token-normalised,
-    then the leak-free causal attention forward.  Returns (O bf16, LSE fp32)."""
+    then the leak-free causal attention forward.  Returns (O bf16, LSE fp32); `o` and `lse` may be
+    given (laid out like q and [B, Hq, S])."""
     qq, qs = mxfp8_quantize_qk_rowwise(q, layout, stream=stream)
     kq, ks = mxfp8_quantize_qk_rowwise(k, layout, stream=stream)
     if leaky:
@@ -191,4 +192,4 @@ def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, stream
     else:
         vt, vsc, vtn, vtn_sc = mxfp8_quantize_v_fused(v, layout, stream=stream)
     return mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, p_terms, leaky,
-                                 stream=stream)
+                                 o=o, lse=lse, stream=stream)

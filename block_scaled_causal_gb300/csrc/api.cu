@@ -41,9 +41,9 @@ bsc_status check_shape(int B, int S, int H, int D, int layout, bool* empty) {
     *empty = true;
     return BSC_OK;
   }
-  if (D != 128 || S % 128 != 0) return BSC_ERR_UNSUPPORTED;
+  if (D != 128 || S % 32 != 0) return BSC_ERR_UNSUPPORTED;
   // every index the kernels form fits in 64 bits; the grids must fit their limits
-  if ((long long)B * H * (S / 128) >= (1LL << 31)) return BSC_ERR_UNSUPPORTED;
+  if ((long long)B * H * ((S + 127) / 128) >= (1LL << 31)) return BSC_ERR_UNSUPPORTED;
   return BSC_OK;
 }
 

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.S / BM;
+  const int T = (a.S + BM - 1) / BM;   // the last tile may hold fewer rows (S is a multiple of 32)
   // heaviest tiles first; the query heads sharing a KV head are adjacent
   const int bh = blockIdx.x % (a.B * a.Hq);
   const int t = T - 1 - (int)(blockIdx.x / (a.B * a.Hq));
@@ -176,9 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (own_split) {
         // the own-block tile of the token-normalised V, decoded early by warps 2-3
         prefetch_tensormap(&a.tm_vtn);
-        mbar_arrive_expect_tx(bar(B_VTN_FULL), BN * HD + BN);
+        // amplitudes of the tile's keys that exist (a multiple of 32); the decode zeroes the rest
+        const uint32_t namp = (uint32_t)min(BN, a.S - t * BN);
+        mbar_arrive_expect_tx(bar(B_VTN_FULL), BN * HD + namp);
         tma_load_4d(sbase + OFF_VTN8, &a.tm_vtn, bar(B_VTN_FULL), 0, hk, t * BN, b);
-        bulk_load(sbase + OFF_VTNSC, a.vtn_sc + kv_plane * a.S + (long long)t * BN, BN, bar(B_VTN_FULL));
+        bulk_load(sbase + OFF_VTNSC, a.vtn_sc + kv_plane * a.S + (long long)t * BN, namp, bar(B_VTN_FULL));
       }
       int nl[NST] = {};   // stage loads issued
       bool ok = true;
@@ -284,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (__all_sync(0xFFFFFFFFu, mbar_wait(bar(B_VTN_FULL), 0, ctl, W_DEC_VTN))) {
         const uint8_t* raw = smem + OFF_VTN8;
         const uint8_t* amp = smem + OFF_VTNSC;
+        const int nkeys = min(BN, a.S - t * BN);   // keys past S: bytes zero-filled, no amplitude
         for (int part = 0; part < 4; ++part) {
           const int d = u + 32 * part;
           for (int kc = 0; kc < 16; ++kc) {
@@ -294,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               const int k0 = 16 * (kc >> 1) + 8 * (e & 1) + 4 * (kc & 1) + 2 * (e >> 1);
               const uint16_t pair = (uint16_t)raw[k0 * HD + d] | ((uint16_t)raw[(k0 + 1) * HD + d] << 8);
               const uint32_t h2 = cvt_e4m3x2_to_f16x2(pair);
-              const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * pow2_e8m0(amp[k0]);
-              const float v1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * pow2_e8m0(amp[k0 + 1]);
+              const float v0 = k0 < nkeys ? __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * pow2_e8m0(amp[k0]) : 0.f;
+              const float v1 = k0 + 1 < nkeys ? __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * pow2_e8m0(amp[k0 + 1]) : 0.f;
               w[e] = pack_bf16x2(v0, v1);
             }
             const uint32_t off = OFF_VT + (kc >> 3) * (HD * 128) + d * 128 + (((kc & 7) ^ (d & 7)) * 16);
@@ -525,9 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int k = e8 * 8 + 2 * e;
           w[e] = pack_bf16x2(o[k >> 5][k & 31] * inv_l, o[(k + 1) >> 5][(k + 1) & 31] * inv_l);
         }
-        orow[e8] = make_uint4(w[0], w[1], w[2], w[3]);
+        if (i < a.S) orow[e8] = make_uint4(w[0], w[1], w[2], w[3]);   // rows past S hold no token
       }
-      if (h == 0) {
+      if (h == 0 && i < a.S) {
         const float ln2 = 0.69314718055994531f;
         a.lse[((long long)b * a.Hq + hq) * a.S + i] = (m_fin + lg2_approx(l) - P_SHIFT) * ln2;
       }
@@ -550,7 +553,7 @@ cudaError_t launch_variant(const AttnArgs& args, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long ctas = (long long)args.B * args.Hq * (args.S / BM);
+  const long long ctas = (long long)args.B * args.Hq * ((args.S + BM - 1) / BM);
   kern<<<(unsigned)ctas, kThreads, SMEM_BYTES, st>>>(args);
   return cudaGetLastError();
 }

@@ -52,8 +52,8 @@ __device__ __forceinline__ uint32_t atom_word_offset(uint32_t m) { return (m & 3
 // ------------------------------------------------------------------------------------------
 // Rowwise quantiser (Q, K): one thread per 16 bytes (8 elements); 16 threads per 128-element row;
 // a 32-element block is 4 adjacent threads.  Rows are visited in memory order; (b, s, h) of a row
-// follows from the layout.  Scale words go to the atom layout
-//   sc[((b*H + h) * (S/128) + s/128) * 512 + (s%32)*16 + ((s%128)/32)*4 + c],  c = d / 32.
+// follows from the layout.  Scale words go to the atom layout, T = ceil(S/128) atoms per (b, h):
+//   sc[((b*H + h) * T + s/128) * 512 + (s%32)*16 + ((s%128)/32)*4 + c],  c = d / 32.
 __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint4* __restrict__ x, uint2* __restrict__ q,
                                                             uint8_t* __restrict__ sc, long long nrows, int B,
                                                             int S, int H, int layout) {
@@ -80,17 +80,29 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint4* __restr
     if (layout == 0) { s = r2 % S; b = r2 / S; }
     else { b = r2 % B; s = r2 / B; }
     const long long plane = b * H + h;
-    const long long off = (plane * (S / 128) + s / 128) * 512 + atom_word_offset((uint32_t)(s & 127));
+    const long long off = (plane * ((S + 127) / 128) + s / 128) * 512 + atom_word_offset((uint32_t)(s & 127));
     *reinterpret_cast<uint32_t*>(sc + off) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
   }
 }
 
+// Rows S..T*128-1 of the last row atom of each (b, h) hold no token: their scale words are 0.
+__global__ void __launch_bounds__(128) pad_row_atoms_kernel(uint8_t* __restrict__ sc, int S) {
+  const int T = (S + 127) / 128;
+  const int s = (T - 1) * 128 + (int)threadIdx.x;
+  if (s >= S) {
+    const long long off = ((long long)blockIdx.x * T + (T - 1)) * 512 + atom_word_offset((uint32_t)(s & 127));
+    *reinterpret_cast<uint32_t*>(sc + off) = 0u;
+  }
+}
+
 // ------------------------------------------------------------------------------------------
-// V quantiser: one CTA per (b, h, 128-token tile), 256 threads.  Produces either or both of
+// V quantiser: one CTA per (b, h, 128-token tile), 256 threads (the last tile of a sequence may
+// hold fewer than 128 tokens, always whole 32-token blocks).  Produces either or both of
 //   * the columnwise copy, transposed, with the tokens of each aligned 32-token block in the order
 //     perm32 (the order the attention kernel's P operand uses, see bsc.h):
 //     vt[((b*H + h)*D + d)*S + 32*blk + x] = token 32*blk + perm32(x), with scale atoms
-//       vsc[((b*H + h)*(S/128) + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32];
+//       vsc[((b*H + h)*T + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32],  T = ceil(S/128)
+//     (the bytes of blocks past S in the last atom are 0);
 //   * the token-normalised copy in V's own layout with scales vtn_sc[(b*H + h)*S + s].
 constexpr int VQ_ROWS = 128;
 constexpr int VQ_PITCH = 256 + 16;   // bytes per staged token row
@@ -100,7 +112,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
                                                       uint8_t* __restrict__ vtn_sc, int B, int S, int H,
                                                       int layout) {
   __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
-  const int ntiles = S / VQ_ROWS;
+  const int ntiles = (S + VQ_ROWS - 1) / VQ_ROWS;
   const int tile_idx = blockIdx.x % ntiles;
   const int plane = blockIdx.x / ntiles;   // b*H + h
   const int h = plane % H, b = plane / H;
@@ -114,10 +126,11 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
   for (int it = 0; it < 8; ++it) {
     const int c = it * 256 + tid;
     const int r = c >> 4, l16 = c & 15;
+    const bool valid = s0 + r < S;   // uniform over the 16 threads of a row
     const long long e = base0 + (long long)(s0 + r) * row_stride + l16 * 8;
-    const uint4 val = __ldcs(reinterpret_cast<const uint4*>(v + e * 2));
+    const uint4 val = valid ? __ldcs(reinterpret_cast<const uint4*>(v + e * 2)) : make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(&tile[r * VQ_PITCH + l16 * 16]) = val;
-    if (vtn != nullptr) {
+    if (vtn != nullptr && valid) {
       // token-normalised copy straight from registers: the 16 threads of a row reduce its amax
       uint32_t am = absmax_bits8(val);
 #pragma unroll
@@ -159,15 +172,18 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
     o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
   }
   const int d0 = 2 * dp, d1 = 2 * dp + 1;
-  uint8_t* row0 = vt + ((long long)plane * 128 + d0) * S + s0 + kb * 32;
-  uint8_t* row1 = vt + ((long long)plane * 128 + d1) * S + s0 + kb * 32;
-  __stcs(reinterpret_cast<uint4*>(row0), make_uint4(o0[0], o0[1], o0[2], o0[3]));
-  __stcs(reinterpret_cast<uint4*>(row0) + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
-  __stcs(reinterpret_cast<uint4*>(row1), make_uint4(o1[0], o1[1], o1[2], o1[3]));
-  __stcs(reinterpret_cast<uint4*>(row1) + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
+  const bool valid = s0 + kb * 32 < S;   // whole 32-token blocks
+  if (valid) {
+    uint8_t* row0 = vt + ((long long)plane * 128 + d0) * S + s0 + kb * 32;
+    uint8_t* row1 = vt + ((long long)plane * 128 + d1) * S + s0 + kb * 32;
+    __stcs(reinterpret_cast<uint4*>(row0), make_uint4(o0[0], o0[1], o0[2], o0[3]));
+    __stcs(reinterpret_cast<uint4*>(row0) + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
+    __stcs(reinterpret_cast<uint4*>(row1), make_uint4(o1[0], o1[1], o1[2], o1[3]));
+    __stcs(reinterpret_cast<uint4*>(row1) + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
+  }
   uint8_t* atom = vsc + ((long long)plane * ntiles + tile_idx) * 512;
-  atom[atom_word_offset(d0) + kb] = (uint8_t)sb0;
-  atom[atom_word_offset(d1) + kb] = (uint8_t)sb1;
+  atom[atom_word_offset(d0) + kb] = valid ? (uint8_t)sb0 : (uint8_t)0;
+  atom[atom_word_offset(d1) + kb] = valid ? (uint8_t)sb1 : (uint8_t)0;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -178,12 +194,13 @@ cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, 
   const unsigned grid = (unsigned)((chunks + 255) / 256);
   quant_rowwise_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(q), sc,
                                               nrows, B, S, H, layout);
+  if (S % 128 != 0) pad_row_atoms_kernel<<<(unsigned)((long long)B * H), 128, 0, st>>>(sc, S);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_v(const void* v, uint8_t* vt, uint8_t* vsc, uint8_t* vtn, uint8_t* vtn_sc, int B, int S,
                            int H, int layout, cudaStream_t st) {
-  const long long ctas = (long long)B * H * (S / VQ_ROWS);
+  const long long ctas = (long long)B * H * ((S + VQ_ROWS - 1) / VQ_ROWS);
   quant_v_kernel<<<(unsigned)ctas, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(v), vt, vsc, vtn, vtn_sc, B, S,
                                                   H, layout);
   return cudaGetLastError();

@@ -15,7 +15,9 @@
  *     synchronises; all work is enqueued on `stream` (NULL = the legacy default stream).
  *   - Arguments are checked before anything is enqueued; on any error nothing is launched.
  *   - Calls hold no state between invocations and may be made from several host threads.
- *   - Tokens S must be a multiple of 128 and D must be 128.  B, S or H equal to 0 is an empty
+ *   - Tokens S must be a multiple of 32 (whole MX blocks) and D must be 128.  Work is tiled by 128
+ *     tokens; T = ceil(S/128) is the number of tiles per (b, h), the last one possibly partial.
+ *     B, S or H equal to 0 is an empty
  *     problem: the call returns BSC_OK and launches nothing (pointers are not inspected).
  *   - Every pointer must be 16-byte aligned.
  *   - The current CUDA device must be compute capability 10.3 (GB300).
@@ -33,11 +35,12 @@
  *                             its 32 tokens.
  *   Scale bytes are E8M0 (value 2^(byte-127); 0xFF = NaN) and come in two forms:
  *   "row atoms" (Q and K rowwise scales):  one byte per (b, h, s, c) with c = d/32, at
- *        ((b*H + h)*(S/128) + s/128)*512 + (s%32)*16 + ((s%128)/32)*4 + c
+ *        ((b*H + h)*T + s/128)*512 + (s%32)*16 + ((s%128)/32)*4 + c
  *   "column atoms" (V columnwise scales): one byte per (b, h, d, 32-token block), at
- *        ((b*H + h)*(S/128) + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32
+ *        ((b*H + h)*T + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32
  *     Both are the 128x4 scale-factor atom order read by the tensor cores (each 512-byte atom
- *     covers 128 rows x 4 blocks of 32), so the attention kernel copies atoms unchanged.
+ *     covers 128 rows x 4 blocks of 32), so the attention kernel copies atoms unchanged.  Both take
+ *     B*H*T*512 bytes; in the last atom of a partial tile the bytes of tokens past S are written 0.
  *   vtn_sc                    token amplitudes, one byte per (b, h, s) at (b*H + h)*S + s
  *   lse                       fp32 [B][Hq][S], natural log
  *
@@ -64,7 +67,7 @@ typedef enum {
   BSC_ERR_NULL = 1,           /* a required pointer is NULL */
   BSC_ERR_SHAPE = 2,          /* negative size, Hq not a multiple of Hkv, bad layout code */
   BSC_ERR_ALIGN = 3,          /* a pointer is not 16-byte aligned */
-  BSC_ERR_UNSUPPORTED = 4,    /* D != 128, S % 128 != 0, wrong device, unsupported option */
+  BSC_ERR_UNSUPPORTED = 4,    /* D != 128, S % 32 != 0, wrong device, unsupported option */
   BSC_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed (launch, tensor map) */
   BSC_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait gave up (see bsc_read_device_status) */
 } bsc_status;
@@ -81,7 +84,7 @@ const char* bsc_status_string(bsc_status s);
  * Rowwise MXFP8 quantisation of Q or K: one E8M0 scale per 32 consecutive elements along D of
  * each (b, s, h) row ("Q/K decoded from their rowwise MXFP8 bytes", PR #3865 Description).
  *   x_bf16 [in]  bf16 in `layout`;  x_e4m3 [out] same layout;  x_sc [out] row atoms,
- *   B*H*S*4 bytes.
+ *   B*H*T*512 bytes.
  */
 bsc_status mxfp8_quantize_qk_rowwise(const void* x_bf16, int B, int S, int H, int D, bsc_layout layout,
                                      uint8_t* x_e4m3, uint8_t* x_sc, bsc_stream_t stream);
@@ -91,7 +94,7 @@ bsc_status mxfp8_quantize_qk_rowwise(const void* x_bf16, int B, int S, int H, in
  * ("A columnwise MXFP8 V scale is shared by 32 consecutive tokens", PR #3865 Description).
  *   v_bf16 [in] bf16 in `layout`;  v_e4m3_t [out] [B][H][D][S] (perm32 order within 32-token
  *   blocks);  v_sc [out] column atoms,
- *   B*H*(S/32)*D bytes.
+ *   B*H*T*512 bytes.
  */
 bsc_status mxfp8_quantize_v_colwise(const void* v_bf16, int B, int S, int H, int D, bsc_layout layout,
                                     uint8_t* v_e4m3_t, uint8_t* v_sc, bsc_stream_t stream);

@@ -53,7 +53,7 @@ FAKE = 0x100000   # 16-byte aligned, never dereferenced: every call below fails 
 
 @pytest.mark.parametrize("args,want", [
     ((FAKE, 1, 128, 2, 64, 0, FAKE, FAKE), 4),       # D != 128
-    ((FAKE, 1, 100, 2, 128, 0, FAKE, FAKE), 4),      # S % 128
+    ((FAKE, 1, 100, 2, 128, 0, FAKE, FAKE), 4),      # S % 32
     ((FAKE, -1, 128, 2, 128, 0, FAKE, FAKE), 2),     # negative size
     ((FAKE, 1, 128, 2, 128, 7, FAKE, FAKE), 2),      # bad layout
     ((None, 1, 128, 2, 128, 0, FAKE, FAKE), 1),      # NULL input
@@ -69,7 +69,7 @@ def test_v_validation(ops):
     L = ops.lib
     assert L.mxfp8_quantize_v_fused(FAKE, 1, 128, 2, 128, 0, FAKE, FAKE, None, FAKE, None) == 1
     assert L.mxfp8_quantize_v_colwise(FAKE, 1, 128, 2, 128, 0, FAKE + 4, FAKE, None) == 3
-    assert L.v_token_normalize(FAKE, 1, 96, 2, 128, 0, FAKE, FAKE, None) == 4
+    assert L.v_token_normalize(FAKE, 1, 80, 2, 128, 0, FAKE, FAKE, None) == 4
     assert L.v_token_normalize(FAKE, 2, 0, 2, 128, 1, None, None, None) == 0
 
 
