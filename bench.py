@@ -231,20 +231,26 @@ def main():
     vtn_sc = torch.empty((B, Hkv, S), **u8)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    o8 = torch.empty(q.shape, **u8)
+    o8_sc = torch.empty((B, Hq, T, 512), **u8)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)   # 256 MB > L2
     stream = torch.cuda.current_stream(dev)
 
-    def step(p_terms, ev_mid):
+    def step(p_terms, ev_mid, out8=False):
         ops.mxfp8_quantize_qk_rowwise(q, w.layout, out=qq, out_sc=qs, stream=stream)
         ops.mxfp8_quantize_qk_rowwise(k, w.layout, out=kq, out_sc=ks, stream=stream)
         ops.mxfp8_quantize_v_fused(v, w.layout, out=(vt, vsc, vtn, vtn_sc), stream=stream)
         ev_mid.record(stream)
-        ops.mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, w.layout, w.scale, p_terms=p_terms,
-                                  o=o, lse=lse, stream=stream)
+        if out8:   # MXFP8 O (E4M3 + one UE8M0 scale per 32 d) instead of BF16 O
+            ops.mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, w.layout, w.scale, p_terms=p_terms,
+                                      lse=lse, stream=stream, o8_out=True, bf16_out=False, o8=o8, o_sc=o8_sc)
+        else:
+            ops.mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, w.layout, w.scale, p_terms=p_terms,
+                                      o=o, lse=lse, stream=stream)
 
-    def timed(p_terms, steps, warmup):
+    def timed(p_terms, steps, warmup, out8=False):
         for _ in range(warmup):
-            step(p_terms, torch.cuda.Event(enable_timing=True))
+            step(p_terms, torch.cuda.Event(enable_timing=True), out8)
         evs = []
         for _ in range(steps):
             flush.zero_()                                   # L2 flushed between steps, outside the events
@@ -252,7 +258,7 @@ def main():
             ev_mid = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step(p_terms, ev_mid)
+            step(p_terms, ev_mid, out8)
             e1.record(stream)
             evs.append((e0, ev_mid, e1))
         return evs
@@ -290,6 +296,11 @@ def main():
     torch.cuda.synchronize()
     ms2 = sum(a.elapsed_time(c) for a, _, c in evs2) / len(evs2)
     attn2 = sum(b.elapsed_time(c) for _, b, c in evs2) / len(evs2)
+    # the same step writing MXFP8 O instead of BF16 O
+    evs8 = timed(args.p_terms, max(3, args.steps // 2), 2, out8=True)
+    torch.cuda.synchronize()
+    ms8 = sum(a.elapsed_time(c) for a, _, c in evs8) / len(evs8)
+    attn8 = sum(b.elapsed_time(c) for _, b, c in evs8) / len(evs8)
 
     # end to end through the public call with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -351,6 +362,7 @@ def main():
         "quant_ms": sum(quant_ms) / len(quant_ms),
         "attn_ms": attn_avg,
         "p_terms2": {"ms_per_step": ms2, "attn_ms": attn2, "value": world * flops / (ms2 * 1e-3) / 1e12},
+        "mxfp8_o": {"ms_per_step": ms8, "attn_ms": attn8, "value": world * flops / (ms8 * 1e-3) / 1e12},
         "wall_s_timed_region": t_wall,
     }
     print(json.dumps(line), flush=True)

@@ -55,6 +55,7 @@ class AttnFwdParams(ctypes.Structure):
         ("p_terms", ctypes.c_int), ("leaky", ctypes.c_int),
         ("dev_status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32),
         ("debug_stall", ctypes.c_int),
+        ("o_e4m3", ctypes.c_void_p), ("o_sc", ctypes.c_void_p),
     ]
 
 
@@ -148,31 +149,44 @@ def mxfp8_quantize_v_fused(v, layout=BSHD, out=None, stream=None):
 
 
 def make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, softmax_scale, p_terms=1, leaky=0,
-                     dev_status=None, wait_timeout_ms=0, debug_stall=0):
+                     dev_status=None, wait_timeout_ms=0, debug_stall=0, o8=None, o_sc=None):
     B, S, Hq, D = _bshd_dims(q, layout)
     Hkv = _bshd_dims(k, layout)[2]
     return AttnFwdParams(q=q.data_ptr(), q_sc=q_sc.data_ptr(), k=k.data_ptr(), k_sc=k_sc.data_ptr(),
                          v_t=v_t.data_ptr(), v_sc=v_sc.data_ptr(),
                          vtn=0 if vtn is None else vtn.data_ptr(), vtn_sc=0 if vtn_sc is None else vtn_sc.data_ptr(),
-                         o=o.data_ptr(), lse=lse.data_ptr(), B=B, S=S, Hq=Hq, Hkv=Hkv, D=D, layout=layout,
-                         softmax_scale=softmax_scale, p_terms=p_terms, leaky=leaky,
+                         o=0 if o is None else o.data_ptr(), lse=lse.data_ptr(), B=B, S=S, Hq=Hq, Hkv=Hkv, D=D,
+                         layout=layout, softmax_scale=softmax_scale, p_terms=p_terms, leaky=leaky,
                          dev_status=0 if dev_status is None else dev_status.data_ptr(),
-                         wait_timeout_ms=wait_timeout_ms, debug_stall=debug_stall)
+                         wait_timeout_ms=wait_timeout_ms, debug_stall=debug_stall,
+                         o_e4m3=0 if o8 is None else o8.data_ptr(), o_sc=0 if o_sc is None else o_sc.data_ptr())
 
 
 def mxfp8_causal_attn_fwd(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, layout=BSHD, softmax_scale=None, p_terms=1,
                           leaky=0, o=None, lse=None, dev_status=None, wait_timeout_ms=0, debug_stall=0,
-                          stream=None):
-    """Leak-free causal MXFP8 attention forward on quantised operands; returns (O bf16, LSE fp32)."""
+                          stream=None, o8_out=False, bf16_out=True, o8=None, o_sc=None):
+    """Leak-free causal MXFP8 attention forward on quantised operands.
+
+    Returns (O bf16, LSE fp32); with o8_out=True, (O bf16 or None, LSE, O E4M3 bytes laid out like
+    q, O row-atom scales [B, Hq, ceil(S/128), 512]).
+    """
     B, S, Hq, D = _bshd_dims(q, layout)
     if softmax_scale is None:
         softmax_scale = D ** -0.5
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if o is None else o
+    if bf16_out:
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if o is None else o
+    else:
+        o = None
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    if o8_out:
+        o8 = torch.empty(q.shape, dtype=torch.uint8, device=q.device) if o8 is None else o8
+        o_sc = torch.empty((B, Hq, (S + 127) // 128, 512), dtype=torch.uint8, device=q.device) if o_sc is None else o_sc
+    else:
+        o8 = o_sc = None
     p = make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, softmax_scale, p_terms, leaky,
-                         dev_status, wait_timeout_ms, debug_stall)
+                         dev_status, wait_timeout_ms, debug_stall, o8, o_sc)
     _check(lib.mxfp8_causal_attn_fwd(ctypes.byref(p), _stream(stream)))
-    return o, lse
+    return (o, lse, o8, o_sc) if o8_out else (o, lse)
 
 
 def bsc_read_device_status(dev_status, stream=None):
@@ -180,10 +194,12 @@ def bsc_read_device_status(dev_status, stream=None):
     return lib.bsc_read_device_status(_ptr(dev_status), _stream(stream))
 
 
-def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, o=None, lse=None, stream=None):
+def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, o=None, lse=None, stream=None,
+            o8_out=False, bf16_out=True):
     """The whole hot path on bf16 inputs: quantise Q, K rowwise, V columnwise + token-normalised,
     then the leak-free causal attention forward.  Returns (O bf16, LSE fp32); `o` and `lse` may be
-    given (laid out like q and [B, Hq, S])."""
+    given (laid out like q and [B, Hq, S]).  With o8_out=True the MXFP8 O is returned as well, as
+    in mxfp8_causal_attn_fwd."""
     qq, qs = mxfp8_quantize_qk_rowwise(q, layout, stream=stream)
     kq, ks = mxfp8_quantize_qk_rowwise(k, layout, stream=stream)
     if leaky:
@@ -192,4 +208,4 @@ def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, o=None
     else:
         vt, vsc, vtn, vtn_sc = mxfp8_quantize_v_fused(v, layout, stream=stream)
     return mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, p_terms, leaky,
-                                 o=o, lse=lse, stream=stream)
+                                 o=o, lse=lse, stream=stream, o8_out=o8_out, bf16_out=bf16_out)

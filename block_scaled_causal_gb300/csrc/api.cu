@@ -112,7 +112,7 @@ bsc_status quant_v_common(const void* v, int B, int S, int H, int D, bsc_layout 
 
 extern "C" {
 
-int bsc_abi_version(void) { return 1; }
+int bsc_abi_version(void) { return 2; }
 
 const char* bsc_status_string(bsc_status s) {
   switch (s) {
@@ -165,9 +165,12 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
   if (p->p_terms != 1 && p->p_terms != 2) return BSC_ERR_UNSUPPORTED;
   if (p->leaky != 0 && p->leaky != 1) return BSC_ERR_UNSUPPORTED;
   const bool own = p->leaky == 0;
-  if (!p->q || !p->q_sc || !p->k || !p->k_sc || !p->v_t || !p->v_sc || !p->o || !p->lse) return BSC_ERR_NULL;
+  if (!p->q || !p->q_sc || !p->k || !p->k_sc || !p->v_t || !p->v_sc || !p->lse) return BSC_ERR_NULL;
+  if (!p->o && !p->o_e4m3) return BSC_ERR_NULL;
+  if (p->o_e4m3 && !p->o_sc) return BSC_ERR_NULL;
   if (own && (!p->vtn || !p->vtn_sc)) return BSC_ERR_NULL;
-  const void* ptrs[] = {p->q, p->q_sc, p->k, p->k_sc, p->v_t, p->v_sc, p->o, p->lse, p->dev_status};
+  const void* ptrs[] = {p->q, p->q_sc, p->k, p->k_sc, p->v_t, p->v_sc, p->o, p->lse, p->dev_status,
+                        p->o_e4m3, p->o_sc};
   for (const void* q : ptrs)
     if (!aligned16(q)) return BSC_ERR_ALIGN;
   if (own && (!aligned16(p->vtn) || !aligned16(p->vtn_sc))) return BSC_ERR_ALIGN;
@@ -185,6 +188,8 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
   a.v_sc = p->v_sc;
   a.vtn_sc = own ? p->vtn_sc : nullptr;
   a.o = p->o;
+  a.o8 = p->o_e4m3;
+  a.o_sc = p->o_sc;
   a.lse = p->lse;
   a.dev_status = p->dev_status;
   a.limit_ns = (unsigned long long)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;

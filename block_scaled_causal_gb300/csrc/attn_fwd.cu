@@ -514,21 +514,56 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const float inv_l = (float)(1 << (int)P_SHIFT) / l;
       const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq
                                           : ((long long)i * a.B + b) * a.Hq + hq;
-      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + row * HD + 64 * h);
       const uint32_t tOb = tmem + T_O + ((uint32_t)(q * 32) << 16) + 64 * h;
       float o[2][32];
       tmem_ld32f(tOb, o[0]);
       tmem_ld32f(tOb + 32, o[1]);
       tmem_ld_wait();
+      const bool row_ok = i < a.S;   // rows past S hold no token
 #pragma unroll
-      for (int e8 = 0; e8 < 8; ++e8) {
-        uint32_t w[4];
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = e8 * 8 + 2 * e;
-          w[e] = pack_bf16x2(o[k >> 5][k & 31] * inv_l, o[(k + 1) >> 5][(k + 1) & 31] * inv_l);
+        for (int e = 0; e < 32; ++e) o[c][e] *= inv_l;
+      }
+      if (a.o != nullptr) {
+        uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + row * HD + 64 * h);
+#pragma unroll
+        for (int e8 = 0; e8 < 8; ++e8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = e8 * 8 + 2 * e;
+            w[e] = pack_bf16x2(o[k >> 5][k & 31], o[(k + 1) >> 5][(k + 1) & 31]);
+          }
+          if (row_ok) orow[e8] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        if (i < a.S) orow[e8] = make_uint4(w[0], w[1], w[2], w[3]);   // rows past S hold no token
+      }
+      if (a.o8 != nullptr) {
+        // MXFP8 O: this thread's 64 columns are the 32-element blocks 2h and 2h + 1 of row r, so each
+        // block maximum is thread-local.  The maximum is taken on |bit patterns| (NaN above Inf above
+        // every finite value); scales go to row r's word of the tile's row atom.
+        uint8_t* atom = a.o_sc + (((long long)b * a.Hq + hq) * T + t) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t mb = 0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mb = max(mb, __float_as_uint(o[c][e]) & 0x7FFFFFFFu);
+          float inv;
+          const uint32_t sbyte = e8m0_from_amax(__uint_as_float(mb), inv);
+          uint32_t wq[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t lo = cvt_e4m3x2(o[c][4 * k] * inv, o[c][4 * k + 1] * inv);
+            const uint32_t hi = cvt_e4m3x2(o[c][4 * k + 2] * inv, o[c][4 * k + 3] * inv);
+            wq[k] = sbyte == 0xFFu ? 0x7F7F7F7Fu : (lo | (hi << 16));
+          }
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(a.o8 + row * HD + 64 * h + 32 * c);
+            dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+            dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+          }
+          atom[2 * h + c] = row_ok ? (uint8_t)sbyte : (uint8_t)0;
+        }
       }
       if (h == 0 && i < a.S) {
         const float ln2 = 0.69314718055994531f;

@@ -21,7 +21,9 @@ struct AttnArgs {
   const uint8_t* k_sc;
   const uint8_t* v_sc;
   const uint8_t* vtn_sc;
-  void* o;
+  void* o;              // bf16 O, or nullptr
+  uint8_t* o8;          // E4M3 O, or nullptr
+  uint8_t* o_sc;        // row atoms of the E4M3 O scales (with o8)
   float* lse;
   int32_t* dev_status;
   unsigned long long limit_ns;

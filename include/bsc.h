@@ -122,7 +122,7 @@ typedef struct {
   const uint8_t* v_sc;    /* [in] V column atoms */
   const uint8_t* vtn;     /* [in] token-normalised V bytes, `layout` (unused when leaky = 1) */
   const uint8_t* vtn_sc;  /* [in] token amplitudes [B][Hkv][S] (unused when leaky = 1) */
-  void* o;                /* [out] bf16 O in `layout`, Hq heads */
+  void* o;                /* [out] bf16 O in `layout`, Hq heads (may be NULL when o_e4m3 is set) */
   float* lse;             /* [out] [B][Hq][S], ln sum_{j<=i} exp(softmax_scale * q_i . k_j) */
   int B, S, Hq, Hkv, D;
   int layout;             /* bsc_layout */
@@ -143,12 +143,21 @@ typedef struct {
   /* Test hook: 1 makes the MMA issuer wait on a barrier nothing arrives on, so the call ends
    * through the wait limit with dev_status set.  Must be 0 in normal use. */
   int debug_stall;
+  /* Optional MXFP8 O ("FROST SDPA fp8: block-scaled O epilogues (NVFP4 / MXFP8) with an sf_o
+   * output", cudnn-frontend PR #1088 and its follow-up #1180, Summary: FP8_E4M3 O with one UE8M0
+   * scale per 32 head-dim elements, scales in the F8_128x4 atom order as per-(b, h) planes).
+   * When o_e4m3 is not NULL the epilogue also writes O as E4M3 bytes in `layout` (Hq heads) and
+   * o_sc as row atoms exactly like Q's scales (B*Hq*T*512 bytes, bytes past S written 0), by the
+   * quantisation rule above applied to the fp32 O before any BF16 rounding.  o_sc is required
+   * with o_e4m3. */
+  uint8_t* o_e4m3;
+  uint8_t* o_sc;
 } bsc_attn_fwd_params;
 
 /*
  * Leak-free causal MXFP8 attention forward (PR #3865 Description: completed-block MXFP8 part,
  * own-block part on the token-normalised V, log-sum-exp merge).  GQA: query head h reads
- * KV head h / (Hq/Hkv).  Returns BF16 O and fp32 LSE.
+ * KV head h / (Hq/Hkv).  Returns BF16 O and/or MXFP8 O, and fp32 LSE.
  */
 bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stream);
 

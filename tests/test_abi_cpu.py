@@ -38,14 +38,15 @@ def test_exports_every_declared_symbol(ops):
 def test_status_strings(ops):
     for code in range(7):
         assert ops.lib.bsc_status_string(code).decode().startswith("BSC_")
-    assert ops.lib.bsc_abi_version() == 1
+    assert ops.lib.bsc_abi_version() == 2
 
 
 def test_params_struct_layout(ops):
     # 10 pointers, 5 ints, layout, float, 2 ints, pointer, uint32, int  (x86-64 / aarch64 LP64)
     P = ops.AttnFwdParams
     assert P.B.offset == 80 and P.softmax_scale.offset == 104 and P.dev_status.offset == 120
-    assert ctypes.sizeof(P) == 136
+    assert P.o_e4m3.offset == 136 and P.o_sc.offset == 144
+    assert ctypes.sizeof(P) == 152
 
 
 FAKE = 0x100000   # 16-byte aligned, never dereferenced: every call below fails validation first
