@@ -143,3 +143,44 @@ def reference_forward(q, k, v, scale, rows=None, chunk=256):
     return causal_attention(mx.dequantize_rowwise(qc, qs), mx.dequantize_rowwise(kc, ks),
                             mx.dequantize_colwise(vcc, vcs), mx.dequantize_token_norm(vtc, vts),
                             scale, rows=rows, chunk=chunk)
+
+
+def causal_attention_bwd(qh, kh, vt, o, lse, do, scale, chunk=256):
+    """Backward of the leak-free causal attention on decoded operands, fp64.
+
+    Follows "[PyTorch] Add causal MXFP8 attention without future-token leakage through V scales"
+    (TransformerEngine PR #3865), Description, Backward: an FP16/BF16 attention backward on Q and
+    K decoded from their rowwise MXFP8 bytes and V decoded from the token-normalised copy, fed
+    with the forward's O and LSE.  With s_ij = scale * <Qh_i, Kh_j> (j <= i):
+        P_ij  = exp(s_ij - LSE_i)
+        dV_j  = sum_i P_ij dO_i               dP_ij = <dO_i, Vt_j>
+        Dlt_i = <dO_i, O_i>                   dS_ij = P_ij (dP_ij - Dlt_i)
+        dQ_i  = scale * sum_j dS_ij Kh_j      dK_j  = scale * sum_i dS_ij Qh_i
+    GQA: dK and dV of a KV head sum over the query heads that read it.
+
+    qh, do, o [B,S,Hq,D]; kh, vt [B,S,Hkv,D]; lse [B,Hq,S].  Returns dq [B,S,Hq,D] and
+    dk, dv [B,S,Hkv,D].
+    """
+    qh, kh, vt, o, lse, do = (np.asarray(a, dtype=np.float64) for a in (qh, kh, vt, o, lse, do))
+    B, S, Hq, D = qh.shape
+    Hkv = kh.shape[2]
+    g = Hq // Hkv
+    dq = np.zeros_like(qh)
+    dk = np.zeros_like(kh)
+    dv = np.zeros_like(vt)
+    for b in range(B):
+        for hq in range(Hq):
+            hk = hq // g
+            dlt = np.sum(do[b, :, hq, :] * o[b, :, hq, :], axis=1)            # [S]
+            for r0 in range(0, S, chunk):
+                ri = np.arange(r0, min(S, r0 + chunk))
+                kmax = int(ri.max()) + 1
+                s = scale * (qh[b, ri, hq, :] @ kh[b, :kmax, hk, :].T)         # [R, kmax]
+                visible = np.arange(kmax)[None, :] <= ri[:, None]
+                p = np.where(visible, np.exp(np.where(visible, s, 0.0) - lse[b, hq, ri][:, None]), 0.0)
+                dv[b, :kmax, hk, :] += p.T @ do[b, ri, hq, :]
+                dp = do[b, ri, hq, :] @ vt[b, :kmax, hk, :].T
+                ds = p * (dp - dlt[ri][:, None])
+                dq[b, ri, hq, :] += scale * (ds @ kh[b, :kmax, hk, :])
+                dk[b, :kmax, hk, :] += scale * (ds.T @ qh[b, ri, hq, :])
+    return dq, dk, dv
