@@ -296,6 +296,25 @@ def main():
     torch.cuda.synchronize()
     ms2 = sum(a.elapsed_time(c) for a, _, c in evs2) / len(evs2)
     attn2 = sum(b.elapsed_time(c) for _, b, c in evs2) / len(evs2)
+    # backward on decoded operands (BF16 MMAs), inputs resident: the forward's O and LSE and a dO
+    g_do = torch.Generator(device="cpu").manual_seed(3)
+    d_o = torch.randn(q.shape, generator=g_do, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    dq_, dk_, dv_ = (torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for t in (q, k, k))
+    step(args.p_terms, torch.cuda.Event(enable_timing=True))     # O, LSE of these inputs
+    for _ in range(2):
+        ops.bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o, lse, d_o, w.layout, w.scale, dq=dq_, dk=dk_, dv=dv_,
+                          stream=stream)
+    bwd_ms = []
+    for _ in range(max(3, args.steps // 4)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ops.bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o, lse, d_o, w.layout, w.scale, dq=dq_, dk=dk_, dv=dv_,
+                          stream=stream)
+        e1.record(stream)
+        bwd_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    bwd_avg = sum(a.elapsed_time(b) for a, b in bwd_ms) / len(bwd_ms)
     # the same step writing MXFP8 O instead of BF16 O
     evs8 = timed(args.p_terms, max(3, args.steps // 2), 2, out8=True)
     torch.cuda.synchronize()
@@ -363,6 +382,9 @@ def main():
         "attn_ms": attn_avg,
         "p_terms2": {"ms_per_step": ms2, "attn_ms": attn2, "value": world * flops / (ms2 * 1e-3) / 1e12},
         "mxfp8_o": {"ms_per_step": ms8, "attn_ms": attn8, "value": world * flops / (ms8 * 1e-3) / 1e12},
+        "bwd": {"bwd_ms": bwd_avg, "fwd_bwd_ms": ms_per_step + bwd_avg,
+                "tflops": world * 2.5 * flops / (bwd_avg * 1e-3) / 1e12,
+                "note": "backward on decoded operands, BF16 MMAs; FLOPs = 2.5 x forward"},
         "wall_s_timed_region": t_wall,
     }
     print(json.dumps(line), flush=True)

@@ -37,6 +37,8 @@ def _load():
     lib.mxfp8_quantize_v_fused.argtypes = [vp, i32, i32, i32, i32, i32, u8p, u8p, u8p, u8p, vp]
     lib.mxfp8_causal_attn_fwd.restype = i32
     lib.mxfp8_causal_attn_fwd.argtypes = [ctypes.POINTER(AttnFwdParams), vp]
+    lib.bf16_attn_bwd.restype = i32
+    lib.bf16_attn_bwd.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
     lib.bsc_read_device_status.restype = i32
     lib.bsc_read_device_status.argtypes = [vp, vp]
     return lib
@@ -56,6 +58,20 @@ class AttnFwdParams(ctypes.Structure):
         ("dev_status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32),
         ("debug_stall", ctypes.c_int),
         ("o_e4m3", ctypes.c_void_p), ("o_sc", ctypes.c_void_p),
+    ]
+
+
+class AttnBwdParams(ctypes.Structure):
+    """Mirror of bsc_attn_bwd_params."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("q_sc", ctypes.c_void_p),
+        ("k", ctypes.c_void_p), ("k_sc", ctypes.c_void_p),
+        ("vtn", ctypes.c_void_p), ("vtn_sc", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("d_o", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("S", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("D", ctypes.c_int), ("layout", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+        ("dev_status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32),
     ]
 
 
@@ -209,3 +225,36 @@ def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, o=None
         vt, vsc, vtn, vtn_sc = mxfp8_quantize_v_fused(v, layout, stream=stream)
     return mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, p_terms, leaky,
                                  o=o, lse=lse, stream=stream, o8_out=o8_out, bf16_out=bf16_out)
+
+
+def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softmax_scale=None, dq=None, dk=None,
+                  dv=None, dev_status=None, wait_timeout_ms=0, stream=None):
+    """Backward on decoded operands (quantised Q, K and token-normalised V, the forward's O, LSE);
+    returns (dQ, dK, dV) in bf16, laid out like q and k."""
+    B, S, Hq, D = _bshd_dims(q, layout)
+    Hkv = _bshd_dims(k, layout)[2]
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    _require(do, torch.bfloat16, "do")
+    _require(o, torch.bfloat16, "o")
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dk is None else dk
+    dv = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dv is None else dv
+    p = AttnBwdParams(q=q.data_ptr(), q_sc=q_sc.data_ptr(), k=k.data_ptr(), k_sc=k_sc.data_ptr(),
+                      vtn=vtn.data_ptr(), vtn_sc=vtn_sc.data_ptr(), o=o.data_ptr(), lse=lse.data_ptr(),
+                      d_o=do.data_ptr(), dq=dq.data_ptr(), dk=dk.data_ptr(), dv=dv.data_ptr(), B=B, S=S, Hq=Hq,
+                      Hkv=Hkv, D=D, layout=layout, softmax_scale=softmax_scale,
+                      dev_status=0 if dev_status is None else dev_status.data_ptr(), wait_timeout_ms=wait_timeout_ms)
+    _check(lib.bf16_attn_bwd(ctypes.byref(p), _stream(stream)))
+    return dq, dk, dv
+
+
+def forward_backward(q, k, v, do, layout=BSHD, softmax_scale=None, stream=None):
+    """Forward (one E4M3 term for P) then the backward on decoded operands; returns
+    (O, LSE, dQ, dK, dV)."""
+    qq, qs = mxfp8_quantize_qk_rowwise(q, layout, stream=stream)
+    kq, ks = mxfp8_quantize_qk_rowwise(k, layout, stream=stream)
+    vt, vsc, vtn, vtn_sc = mxfp8_quantize_v_fused(v, layout, stream=stream)
+    o, lse = mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, stream=stream)
+    dq, dk, dv = bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o, lse, do, layout, softmax_scale, stream=stream)
+    return o, lse, dq, dk, dv

@@ -78,6 +78,23 @@ bool encode_tokens_map(CUtensorMap* m, const void* base, int B, int S, int H, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 [.., S, .., H, 128] tensor as a 4-D map {D, H, S, B} with a 128-token x 64-element box
+// (128 bytes, the swizzle span): two boxes cover a row's 128 elements.
+bool encode_bf16_tokens_map(CUtensorMap* m, const void* base, int B, int S, int H, int layout) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  const cuuint64_t sH = 256;
+  const cuuint64_t sS = layout == BSC_BSHD ? (cuuint64_t)H * 256 : (cuuint64_t)B * H * 256;
+  const cuuint64_t sB = layout == BSC_BSHD ? (cuuint64_t)S * H * 256 : (cuuint64_t)H * 256;
+  const cuuint64_t strides[3] = {sH, sS, sB};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Transposed V bytes [rows = B*H*D][S] as a 2-D map with a 128-key x 128-row box.
 bool encode_vt_map(CUtensorMap* m, const void* base, long long rows, int S) {
   auto enc = get_encode();
@@ -203,6 +220,52 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
   a.leaky = p->leaky;
   a.inject_stall = p->debug_stall ? 1 : 0;
   return from_cuda(bsc::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
+  if (!p) return BSC_ERR_NULL;
+  if (p->Hq < 0 || p->Hkv < 0) return BSC_ERR_SHAPE;
+  bool empty;
+  bsc_status s = check_shape(p->B, p->S, p->Hq, p->D, p->layout, &empty);
+  if (s != BSC_OK) return s;
+  if (!empty && p->Hkv == 0) return BSC_ERR_SHAPE;
+  if (empty) return BSC_OK;
+  if (p->Hq % p->Hkv != 0) return BSC_ERR_SHAPE;
+  if (!p->q || !p->q_sc || !p->k || !p->k_sc || !p->vtn || !p->vtn_sc || !p->o || !p->lse || !p->d_o || !p->dq ||
+      !p->dk || !p->dv)
+    return BSC_ERR_NULL;
+  const void* ptrs[] = {p->q, p->q_sc, p->k, p->k_sc, p->vtn, p->vtn_sc, p->o, p->lse, p->d_o, p->dq, p->dk, p->dv,
+                        p->dev_status};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return BSC_ERR_ALIGN;
+  if ((s = check_device()) != BSC_OK) return s;
+
+  bsc::BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_tokens_map(&a.tm_q, p->q, p->B, p->S, p->Hq, p->layout, true) ||
+      !encode_tokens_map(&a.tm_k, p->k, p->B, p->S, p->Hkv, p->layout, true) ||
+      !encode_tokens_map(&a.tm_vtn, p->vtn, p->B, p->S, p->Hkv, p->layout, false) ||
+      !encode_bf16_tokens_map(&a.tm_do, p->d_o, p->B, p->S, p->Hq, p->layout))
+    return BSC_ERR_CUDA;
+  a.q_sc = p->q_sc;
+  a.k_sc = p->k_sc;
+  a.vtn_sc = p->vtn_sc;
+  a.o = p->o;
+  a.dO = p->d_o;
+  a.lse = p->lse;
+  a.dq = p->dq;
+  a.dk = p->dk;
+  a.dv = p->dv;
+  a.dev_status = p->dev_status;
+  a.limit_ns = (unsigned long long)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
+  a.B = p->B;
+  a.S = p->S;
+  a.Hq = p->Hq;
+  a.Hkv = p->Hkv;
+  a.layout = p->layout;
+  a.scale = p->softmax_scale;
+  a.scale_log2e = (float)((double)p->softmax_scale * 1.4426950408889634);
+  return from_cuda(bsc::launch_attn_bwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 bsc_status bsc_read_device_status(const int32_t* dev_status, bsc_stream_t stream) {

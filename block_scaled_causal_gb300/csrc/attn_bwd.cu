@@ -1,0 +1,571 @@
+// Backward of the leak-free causal MXFP8 attention, on decoded operands, with BF16 tensor-core MMAs.
+//
+// "[PyTorch] Add causal MXFP8 attention without future-token leakage through V scales"
+// (TransformerEngine PR #3865), Description, Backward: an FP16/BF16 attention backward on Q and K
+// decoded from their rowwise MXFP8 bytes and V decoded from the token-normalised copy, fed with
+// the forward's O and LSE, so no gradient depends on a future token.  With s = scale * Qh Kh^T:
+//   P = exp(s - LSE),  dV = P^T dO,  dP = dO Vt^T,  Dlt = rowsum(dO * O),  dS = P * (dP - Dlt),
+//   dQ = scale * dS Kh,  dK = scale * dS^T Qh;  a KV head's dK, dV sum over its query heads.
+//
+// Two kernels, 256 threads (8 warps) each, one CTA per SM:
+//   * dK/dV: one CTA per (batch, KV head, 128-key tile); loops over the group's query heads and
+//     the query tiles at or after the key tile, accumulating dV and dK in tensor memory;
+//   * dQ: one CTA per (batch, query head, 128-row query tile); loops over the key tiles up to the
+//     diagonal, accumulating dQ in tensor memory.
+// S = Qh Kh^T is one block-scaled E4M3 MMA on the MXFP8 bytes and scales (exact products); dP, dV,
+// dK and dQ are BF16 MMAs.  Every operand is K-major in shared memory with the 128-byte swizzle;
+// the transposed operands (Q^T, dO^T, K^T, P^T, dS^T) are written there by the threads.  Each
+// iteration runs its phases in turn (loads, decodes, MMAs, elementwise), all threads taking part;
+// thread 0 issues the copies and MMAs.  Every wait is bounded.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "bsc_internal.h"
+#include "ptx.cuh"
+
+namespace bsc {
+namespace {
+
+constexpr int BM = 128;   // query rows per tile
+constexpr int BN = 128;   // keys per tile
+constexpr int HD = 128;   // head dimension
+constexpr int kThreads = 256;
+constexpr uint32_t ATOM = 128 * 128;   // one 128-row x 128-byte swizzle atom column
+
+// TMEM columns: S, dP and two accumulators.  In the dK/dV kernel the scale factors of the S MMA
+// sit at the start of dP's columns; dP is issued only once the S MMA has completed.
+constexpr uint32_t T_S = 0, T_DP = 128, T_ACC0 = 256, T_ACC1 = 384;
+
+enum Bar : uint32_t { B_KV = 0, B_QD, B_MMA1, B_MMA2, B_MMA3, B_DRAIN, B_COUNT };
+enum Site : int { W_KV = 0x20, W_QD, W_MMA1, W_MMA2, W_MMA3 };
+
+// A wait's outcome made the same for every thread of the CTA (the TMEM loads are warp-collective).
+__device__ __forceinline__ bool cta_all(bool ok) { return __syncthreads_and(ok ? 1 : 0) != 0; }
+
+// Byte offset of (row, byte column) inside a K-major tile with 128-byte rows, 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw(uint32_t row, uint32_t colb) {
+  return row * 128u + ((((colb >> 4) ^ row) & 7u) << 4) + (colb & 15u);
+}
+// Byte offset of BF16 element (row, col) of a 128-row x 128-column K-major tile (two atoms).
+__device__ __forceinline__ uint32_t bf_off(uint32_t row, uint32_t col) {
+  return (col >> 6) * ATOM + sw(row, (col & 63u) * 2u);
+}
+__device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
+  return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);   // 2^(sb-127)
+}
+// E4M3 byte pair -> two floats.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t pair) {
+  const uint32_t h2 = cvt_e4m3x2_to_f16x2(pair);
+  return make_float2(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))),
+                     __half2float(__ushort_as_half((unsigned short)(h2 >> 16))));
+}
+// Row atom byte of (row, 32-element block) in a 512-byte scale atom.
+__device__ __forceinline__ uint32_t atom_byte(uint32_t row, uint32_t blk) {
+  return (row & 31u) * 16u + ((row >> 5) & 3u) * 4u + blk;
+}
+
+// Row statistics of the 128 query rows of tile `it`: LSE in log2 units and Dlt = <dO_i, O_i>.
+// Two threads per row, 64 head-dim elements each.  Rows past S get LSE = +inf and Dlt = 0, which
+// makes their P and dS exactly 0.
+__device__ __forceinline__ void row_stats(const BwdArgs& a, int b, int hq, int it, float* lse2, float* dlt) {
+  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int i = it * BM + r;
+  float acc = 0.f;
+  if (i < a.S) {
+    const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq : ((long long)i * a.B + b) * a.Hq + hq;
+    const uint4* po = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + row * HD + 64 * half);
+    const uint4* pd = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + row * HD + 64 * half);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 x = __ldg(po + c), y = __ldg(pd + c);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+  if (half == 0) {
+    dlt[r] = i < a.S ? acc : 0.f;
+    lse2[r] = i < a.S ? a.lse[((long long)b * a.Hq + hq) * a.S + i] * 1.4426950408889634f : INFINITY;
+  }
+}
+
+// E4M3 tile [row][d] (TMA, 128-byte swizzle) with row-atom scales -> BF16 transposed [d][row]
+// (K-major with rows = d).  Rows at or past `nrows` become 0.
+__device__ __forceinline__ void decode_transpose(const uint8_t* src8, const uint8_t* sc_atom, uint8_t* dst, int nrows) {
+  for (int unit = threadIdx.x; unit < HD * (BM / 8); unit += kThreads) {
+    const int d = unit & (HD - 1), r0 = (unit >> 7) * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int ra = r0 + 2 * e, rb = ra + 1;
+      const uint16_t pair = (uint16_t)src8[sw(ra, d)] | ((uint16_t)src8[sw(rb, d)] << 8);
+      const float2 f = e4m3x2_to_f2(pair);
+      const float va = ra < nrows ? f.x * pow2_e8m0(sc_atom[atom_byte(ra, d >> 5)]) : 0.f;
+      const float vb = rb < nrows ? f.y * pow2_e8m0(sc_atom[atom_byte(rb, d >> 5)]) : 0.f;
+      w[e] = pack_bf16x2(va, vb);
+    }
+    *reinterpret_cast<uint4*>(dst + bf_off(d, r0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Token-normalised V bytes [key][d] (TMA, no swizzle) with one amplitude per key -> BF16 [key][d].
+// Keys at or past `nkeys` become 0.
+__device__ __forceinline__ void decode_vt(const uint8_t* raw, const uint8_t* amp, uint8_t* dst, int nkeys) {
+  for (int unit = threadIdx.x; unit < BN * (HD / 8); unit += kThreads) {
+    const int key = unit >> 4, d0 = (unit & 15) * 8;
+    const uint2 bytes = *reinterpret_cast<const uint2*>(raw + key * HD + d0);
+    const float s = key < nkeys ? pow2_e8m0(amp[key]) : 0.f;
+    const uint32_t bw[2] = {bytes.x, bytes.y};
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = e4m3x2_to_f2((uint16_t)(bw[e >> 1] >> (16 * (e & 1))));
+      w[e] = pack_bf16x2(f.x * s, f.y * s);
+    }
+    *reinterpret_cast<uint4*>(dst + bf_off(key, d0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// BF16 tile [row][d] (two 64-column swizzle atoms) -> transposed [d][row].
+__device__ __forceinline__ void transpose_bf16(const uint8_t* src, uint8_t* dst) {
+  for (int unit = threadIdx.x; unit < HD * (BM / 8); unit += kThreads) {
+    const int d = unit & (HD - 1), r0 = (unit >> 7) * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t lo = *reinterpret_cast<const uint16_t*>(src + bf_off(r0 + 2 * e, d));
+      const uint32_t hi = *reinterpret_cast<const uint16_t*>(src + bf_off(r0 + 2 * e + 1, d));
+      w[e] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + bf_off(d, r0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Sixteen BF16 MMAs of K = 16 over a 128-deep contraction: D (+)= A B^T, A and B K-major tiles of
+// two swizzle atoms each.
+__device__ __forceinline__ void mma_bf16_k128(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, bool accumulate) {
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    mma_f16_ss(d_tmem, desc_kmajor_sw128(a_smem + (s >> 2) * ATOM + (s & 3) * 32),
+               desc_kmajor_sw128(b_smem + (s >> 2) * ATOM + (s & 3) * 32), idesc_bf16(BM, BN),
+               (accumulate || s > 0) ? 1u : 0u);
+  }
+}
+// S = Qh Kh^T from E4M3 tiles and row-atom scales (copied to TMEM columns t_sf.. first).
+__device__ __forceinline__ void mma_s(uint32_t tmem, uint32_t t_sf, uint32_t q8, uint32_t k8, uint32_t sfq,
+                                      uint32_t sfk) {
+  tc_cp_32x128b_warpx4(tmem + t_sf, desc_sf_block(sfq));
+  tc_cp_32x128b_warpx4(tmem + t_sf + 4, desc_sf_block(sfk));
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    mma_mxf8_ss(tmem + T_S, desc_kmajor_sw128(q8 + kk * 32), desc_kmajor_sw128(k8 + kk * 32),
+                idesc_mxf8(BM, BN, kk, kk), tmem + t_sf, tmem + t_sf + 4, kk > 0 ? 1u : 0u);
+  }
+}
+
+// One thread's view of a 16x256b TMEM load: rows ra = base + lane/4 and rb = ra + 8, keys
+// 8k + 2(lane%4) + e at v[4k + e] (row ra) and v[4k + 2 + e] (row rb).
+struct RowView {
+  int base, ra, rb, qd;
+  uint32_t lane_off;
+};
+__device__ __forceinline__ RowView row_view() {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  RowView v;
+  v.base = (warp & 3) * 32 + (warp >> 2) * 16;
+  v.ra = v.base + (lane >> 2);
+  v.rb = v.ra + 8;
+  v.qd = lane & 3;
+  v.lane_off = (uint32_t)v.base << 16;
+  return v;
+}
+
+// P = exp(s - LSE) of this thread's 64 elements from S in TMEM (row statistics in shared memory);
+// in the diagonal tile keys after the row are masked.
+__device__ __forceinline__ void compute_p(uint32_t tmem, const RowView& rv, const float* lse2, float sl2, bool diag,
+                                          float (&p)[64]) {
+  tmem_ld16x256_x16(tmem + T_S + rv.lane_off, p);
+  tmem_ld_wait();
+  const float la = lse2[rv.ra], lb = lse2[rv.rb];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = 8 * k + 2 * rv.qd + e;
+      p[4 * k + e] = (diag && key > rv.ra) ? 0.f : ex2_approx(fmaf(p[4 * k + e], sl2, -la));
+      p[4 * k + 2 + e] = (diag && key > rv.rb) ? 0.f : ex2_approx(fmaf(p[4 * k + 2 + e], sl2, -lb));
+    }
+  }
+}
+// dS = P (dP - Dlt) from dP in TMEM.
+__device__ __forceinline__ void compute_ds(uint32_t tmem, const RowView& rv, const float* dlt, const float (&p)[64],
+                                           float (&ds)[64]) {
+  tmem_ld16x256_x16(tmem + T_DP + rv.lane_off, ds);
+  tmem_ld_wait();
+  const float da = dlt[rv.ra], db = dlt[rv.rb];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      ds[4 * k + e] = p[4 * k + e] * (ds[4 * k + e] - da);
+      ds[4 * k + 2 + e] = p[4 * k + 2 + e] * (ds[4 * k + 2 + e] - db);
+    }
+  }
+}
+
+// Epilogue: an accumulator (128 rows x 128 columns fp32 in TMEM) times `mul` -> BF16 rows of a
+// tensor laid out like Q (BSHD/SBHD with H heads); rows at or past S are not written.
+__device__ __forceinline__ void store_acc(uint32_t tmem_acc, void* out, const BwdArgs& a, int H, int b, int h,
+                                          int tile, float mul) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qq = warp & 3, half = warp >> 2;
+  const int r = qq * 32 + lane;
+  const int i = tile * BM + r;
+  float o[2][32];
+  const uint32_t ta = tmem_acc + ((uint32_t)(qq * 32) << 16) + 64 * half;
+  tmem_ld32f(ta, o[0]);
+  tmem_ld32f(ta + 32, o[1]);
+  tmem_ld_wait();
+  if (i >= a.S) return;
+  const long long row = a.layout == 0 ? ((long long)b * a.S + i) * H + h : ((long long)i * a.B + b) * H + h;
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + row * HD + 64 * half);
+#pragma unroll
+  for (int e8 = 0; e8 < 8; ++e8) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = e8 * 8 + 2 * e;
+      w[e] = pack_bf16x2(o[k >> 5][k & 31] * mul, o[(k + 1) >> 5][(k + 1) & 31] * mul);
+    }
+    dst[e8] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// ================================================================================================
+// dK, dV.  Shared memory (bytes from a 1024-aligned base):
+constexpr uint32_t KV_K8 = 0;                 // K bytes [key][d], swizzled
+constexpr uint32_t KV_VN8 = KV_K8 + 16384;    // token-normalised V bytes [key][d]
+constexpr uint32_t KV_V = KV_VN8 + 16384;     // V bf16 [key][d]
+constexpr uint32_t KV_Q8 = KV_V + 32768;      // Q bytes [q][d], swizzled
+constexpr uint32_t KV_QT = KV_Q8 + 16384;     // Q^T bf16 [d][q]
+constexpr uint32_t KV_DO = KV_QT + 32768;     // dO bf16 [q][d]; then dS^T bf16 [key][q]
+constexpr uint32_t KV_DOT = KV_DO + 32768;    // dO^T bf16 [d][q]
+constexpr uint32_t KV_PT = KV_DOT + 32768;    // P^T bf16 [key][q]
+constexpr uint32_t KV_SFQ = KV_PT + 32768;
+constexpr uint32_t KV_SFK = KV_SFQ + 512;
+constexpr uint32_t KV_AMP = KV_SFK + 512;
+constexpr uint32_t KV_LSE = KV_AMP + 128;
+constexpr uint32_t KV_DLT = KV_LSE + 512;
+constexpr uint32_t KV_BAR = KV_DLT + 512;
+constexpr uint32_t KV_MISC = KV_BAR + 64;
+constexpr uint32_t KV_SMEM = KV_MISC + 16 + 1024;
+static_assert(KV_SMEM <= 227 * 1024, "shared memory budget");
+
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](uint32_t i) { return sbase + KV_BAR + 8u * i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + KV_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_MISC + 4);
+  float* lse2 = reinterpret_cast<float*>(smem + KV_LSE);
+  float* dlt = reinterpret_cast<float*>(smem + KV_DLT);
+
+  const int T = (a.S + BN - 1) / BN;
+  const int g = a.Hq / a.Hkv;
+  // key tiles with the most query tiles first
+  const int bh = blockIdx.x % (a.B * a.Hkv);
+  const int jt = (int)(blockIdx.x / (a.B * a.Hkv));
+  const int hk = bh % a.Hkv, b = bh / a.Hkv;
+  const long long kv_plane = (long long)b * a.Hkv + hk;
+  const int nkeys = min(BN, a.S - jt * BN);
+
+  if (threadIdx.x == 0) {
+    for (uint32_t i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if ((threadIdx.x >> 5) == 0) {
+    tmem_alloc(sbase + KV_MISC, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, a.dev_status, a.limit_ns};
+  const bool leader = threadIdx.x == 0;
+  bool ok = true;
+
+  // this CTA's K and V tiles
+  const uint32_t namp = (uint32_t)nkeys;
+  if (leader) {
+    mbar_arrive_expect_tx(bar(B_KV), 2 * BN * HD + 512 + namp);
+    tma_load_4d(sbase + KV_K8, &a.tm_k, bar(B_KV), 0, hk, jt * BN, b);
+    bulk_load(sbase + KV_SFK, a.k_sc + (kv_plane * T + jt) * 512, 512, bar(B_KV));
+    tma_load_4d(sbase + KV_VN8, &a.tm_vtn, bar(B_KV), 0, hk, jt * BN, b);
+    bulk_load(sbase + KV_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, namp, bar(B_KV));
+  }
+  ok = cta_all(mbar_wait(bar(B_KV), 0, ctl, W_KV));
+  bool kv_seen = ok;
+  if (ok) decode_vt(smem + KV_VN8, smem + KV_AMP, smem + KV_V, nkeys);
+
+  const RowView rv = row_view();
+  int iter = 0, qd_issued = 0, qd_seen = 0;
+  for (int hq = hk * g; hq < hk * g + g; ++hq) {
+    for (int it = jt; it < T; ++it, ++iter) {
+      const uint32_t par = (uint32_t)iter & 1u;
+      if (leader && ok) {
+        mbar_arrive_expect_tx(bar(B_QD), BM * HD + 512 + 2 * BM * HD);
+        tma_load_4d(sbase + KV_Q8, &a.tm_q, bar(B_QD), 0, hq, it * BM, b);
+        bulk_load(sbase + KV_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + it) * 512, 512, bar(B_QD));
+        tma_load_4d(sbase + KV_DO, &a.tm_do, bar(B_QD), 0, hq, it * BM, b);
+        tma_load_4d(sbase + KV_DO + ATOM, &a.tm_do, bar(B_QD), 64, hq, it * BM, b);
+      }
+      if (ok) ++qd_issued;
+      row_stats(a, b, hq, it, lse2, dlt);
+      if (ok) ok = mbar_wait(bar(B_QD), par, ctl, W_QD);
+      ok = cta_all(ok);
+      if (ok) ++qd_seen;
+      if (ok) {
+        decode_transpose(smem + KV_Q8, smem + KV_SFQ, smem + KV_QT, min(BM, a.S - it * BM));
+        transpose_bf16(smem + KV_DO, smem + KV_DOT);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      // S first: its scale factors occupy dP's first columns until it has completed
+      if (leader && ok) {
+        mma_s(tmem, T_DP, sbase + KV_Q8, sbase + KV_K8, sbase + KV_SFQ, sbase + KV_SFK);
+        tc_commit(bar(B_MMA1));
+      }
+      if (ok) ok = mbar_wait(bar(B_MMA1), par, ctl, W_MMA1);
+      ok = cta_all(ok);
+      tc_fence_after();
+      if (leader && ok) {
+        mma_bf16_k128(tmem + T_DP, sbase + KV_DO, sbase + KV_V, false);   // dP = dO V^T
+        tc_commit(bar(B_MMA3));
+      }
+      float p[64];
+      if (ok) {
+        compute_p(tmem, rv, lse2, a.scale_log2e, it == jt, p);
+        uint8_t* pt = smem + KV_PT;   // P^T [key][q]
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = 8 * k + 2 * rv.qd + e;
+            *reinterpret_cast<__nv_bfloat16*>(pt + bf_off(key, rv.ra)) = __float2bfloat16_rn(p[4 * k + e]);
+            *reinterpret_cast<__nv_bfloat16*>(pt + bf_off(key, rv.rb)) = __float2bfloat16_rn(p[4 * k + 2 + e]);
+          }
+        }
+      }
+      if (ok) ok = mbar_wait(bar(B_MMA3), par, ctl, W_MMA3);
+      ok = cta_all(ok);
+      tc_fence_after();
+      if (ok) {
+        float ds[64];
+        compute_ds(tmem, rv, dlt, p, ds);
+        uint8_t* dst = smem + KV_DO;   // dS^T [key][q] over dO, which the dP MMA has read
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = 8 * k + 2 * rv.qd + e;
+            *reinterpret_cast<__nv_bfloat16*>(dst + bf_off(key, rv.ra)) = __float2bfloat16_rn(ds[4 * k + e]);
+            *reinterpret_cast<__nv_bfloat16*>(dst + bf_off(key, rv.rb)) = __float2bfloat16_rn(ds[4 * k + 2 + e]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (leader && ok) {
+        mma_bf16_k128(tmem + T_ACC0, sbase + KV_PT, sbase + KV_DOT, iter > 0);   // dV += P^T dO
+        mma_bf16_k128(tmem + T_ACC1, sbase + KV_DO, sbase + KV_QT, iter > 0);    // dK += dS^T Q
+        tc_commit(bar(B_MMA2));
+      }
+      if (ok) ok = mbar_wait(bar(B_MMA2), par, ctl, W_MMA2);
+      ok = cta_all(ok);
+      tc_fence_after();
+    }
+  }
+  if (ok && iter > 0) {
+    store_acc(tmem + T_ACC0, a.dv, a, a.Hkv, b, hk, jt, 1.0f);
+    store_acc(tmem + T_ACC1, a.dk, a, a.Hkv, b, hk, jt, a.scale);
+  }
+  if (leader) {
+    // every tcgen05 operation and copy this thread issued must finish before the CTA exits
+    tc_commit(bar(B_DRAIN));
+    mbar_wait_drain(bar(B_DRAIN), 0, a.limit_ns);
+    if (!kv_seen) mbar_wait_drain(bar(B_KV), 0, a.limit_ns);
+    if (qd_issued > qd_seen) mbar_wait_drain(bar(B_QD), (uint32_t)(qd_issued - 1) & 1u, a.limit_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(tmem, 512);
+}
+
+// ================================================================================================
+// dQ.  Shared memory:
+constexpr uint32_t QQ_Q8 = 0;                 // Q bytes [q][d], swizzled
+constexpr uint32_t QQ_DO = QQ_Q8 + 16384;     // dO bf16 [q][d]
+constexpr uint32_t QQ_K8 = QQ_DO + 32768;     // K bytes [key][d], swizzled
+constexpr uint32_t QQ_VN8 = QQ_K8 + 16384;    // token-normalised V bytes [key][d]
+constexpr uint32_t QQ_KT = QQ_VN8 + 16384;    // K^T bf16 [d][key]
+constexpr uint32_t QQ_V = QQ_KT + 32768;      // V bf16 [key][d]
+constexpr uint32_t QQ_DS = QQ_V + 32768;      // dS bf16 [q][key]
+constexpr uint32_t QQ_SFQ = QQ_DS + 32768;
+constexpr uint32_t QQ_SFK = QQ_SFQ + 512;
+constexpr uint32_t QQ_AMP = QQ_SFK + 512;
+constexpr uint32_t QQ_LSE = QQ_AMP + 128;
+constexpr uint32_t QQ_DLT = QQ_LSE + 512;
+constexpr uint32_t QQ_BAR = QQ_DLT + 512;
+constexpr uint32_t QQ_MISC = QQ_BAR + 64;
+constexpr uint32_t QQ_SMEM = QQ_MISC + 16 + 1024;
+static_assert(QQ_SMEM <= 227 * 1024, "shared memory budget");
+
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](uint32_t i) { return sbase + QQ_BAR + 8u * i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + QQ_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + QQ_MISC + 4);
+  float* lse2 = reinterpret_cast<float*>(smem + QQ_LSE);
+  float* dlt = reinterpret_cast<float*>(smem + QQ_DLT);
+
+  const int T = (a.S + BM - 1) / BM;
+  const int bh = blockIdx.x % (a.B * a.Hq);
+  const int it = T - 1 - (int)(blockIdx.x / (a.B * a.Hq));   // heaviest query tiles first
+  const int hq = bh % a.Hq, b = bh / a.Hq;
+  const int hk = hq / (a.Hq / a.Hkv);
+  const long long kv_plane = (long long)b * a.Hkv + hk;
+
+  if (threadIdx.x == 0) {
+    for (uint32_t i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if ((threadIdx.x >> 5) == 0) {
+    tmem_alloc(sbase + QQ_MISC, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, a.dev_status, a.limit_ns};
+  const bool leader = threadIdx.x == 0;
+  bool ok = true;
+
+  if (leader) {
+    mbar_arrive_expect_tx(bar(B_QD), BM * HD + 512 + 2 * BM * HD);
+    tma_load_4d(sbase + QQ_Q8, &a.tm_q, bar(B_QD), 0, hq, it * BM, b);
+    bulk_load(sbase + QQ_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + it) * 512, 512, bar(B_QD));
+    tma_load_4d(sbase + QQ_DO, &a.tm_do, bar(B_QD), 0, hq, it * BM, b);
+    tma_load_4d(sbase + QQ_DO + ATOM, &a.tm_do, bar(B_QD), 64, hq, it * BM, b);
+  }
+  row_stats(a, b, hq, it, lse2, dlt);
+  ok = cta_all(mbar_wait(bar(B_QD), 0, ctl, W_QD));
+  const bool qd_seen = ok;
+
+  const RowView rv = row_view();
+  int kv_issued = 0, kv_seen = 0;
+  for (int jt = 0; jt <= it; ++jt) {
+    const uint32_t par = (uint32_t)jt & 1u;
+    const int nkeys = min(BN, a.S - jt * BN);
+    if (leader && ok) {
+      mbar_arrive_expect_tx(bar(B_KV), 2 * BN * HD + 512 + (uint32_t)nkeys);
+      tma_load_4d(sbase + QQ_K8, &a.tm_k, bar(B_KV), 0, hk, jt * BN, b);
+      bulk_load(sbase + QQ_SFK, a.k_sc + (kv_plane * T + jt) * 512, 512, bar(B_KV));
+      tma_load_4d(sbase + QQ_VN8, &a.tm_vtn, bar(B_KV), 0, hk, jt * BN, b);
+      bulk_load(sbase + QQ_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, (uint32_t)nkeys, bar(B_KV));
+    }
+    if (ok) ++kv_issued;
+    if (ok) ok = mbar_wait(bar(B_KV), par, ctl, W_KV);
+    ok = cta_all(ok);
+    if (ok) ++kv_seen;
+    if (ok) {
+      decode_vt(smem + QQ_VN8, smem + QQ_AMP, smem + QQ_V, nkeys);
+      decode_transpose(smem + QQ_K8, smem + QQ_SFK, smem + QQ_KT, nkeys);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (leader && ok) {
+      mma_s(tmem, T_ACC1, sbase + QQ_Q8, sbase + QQ_K8, sbase + QQ_SFQ, sbase + QQ_SFK);
+      mma_bf16_k128(tmem + T_DP, sbase + QQ_DO, sbase + QQ_V, false);   // dP = dO V^T
+      tc_commit(bar(B_MMA1));
+    }
+    if (ok) ok = mbar_wait(bar(B_MMA1), par, ctl, W_MMA1);
+    ok = cta_all(ok);
+    tc_fence_after();
+    if (ok) {
+      float p[64], ds[64];
+      compute_p(tmem, rv, lse2, a.scale_log2e, jt == it, p);
+      compute_ds(tmem, rv, dlt, p, ds);
+      // dS [q][key]: keys 8k + 2qd and 8k + 2qd + 1 are adjacent, one 32-bit store per pair
+      uint8_t* dsm = smem + QQ_DS;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int key = 8 * k + 2 * rv.qd;
+        *reinterpret_cast<uint32_t*>(dsm + bf_off(rv.ra, key)) = pack_bf16x2(ds[4 * k], ds[4 * k + 1]);
+        *reinterpret_cast<uint32_t*>(dsm + bf_off(rv.rb, key)) = pack_bf16x2(ds[4 * k + 2], ds[4 * k + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (leader && ok) {
+      mma_bf16_k128(tmem + T_ACC0, sbase + QQ_DS, sbase + QQ_KT, jt > 0);   // dQ += dS K
+      tc_commit(bar(B_MMA2));
+    }
+    if (ok) ok = mbar_wait(bar(B_MMA2), par, ctl, W_MMA2);
+    ok = cta_all(ok);
+    tc_fence_after();
+  }
+  if (ok) store_acc(tmem + T_ACC0, a.dq, a, a.Hq, b, hq, it, a.scale);
+  if (leader) {
+    tc_commit(bar(B_DRAIN));
+    mbar_wait_drain(bar(B_DRAIN), 0, a.limit_ns);
+    if (!qd_seen) mbar_wait_drain(bar(B_QD), 0, a.limit_ns);
+    if (kv_issued > kv_seen) mbar_wait_drain(bar(B_KV), (uint32_t)(kv_issued - 1) & 1u, a.limit_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st) {
+  static bool attr_set = false;   // the attribute is per function and per process
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QQ_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long T = (args.S + BM - 1) / BM;
+  attn_bwd_dq_kernel<<<(unsigned)((long long)args.B * args.Hq * T), kThreads, QQ_SMEM, st>>>(args);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_bwd_dkdv_kernel<<<(unsigned)((long long)args.B * args.Hkv * T), kThreads, KV_SMEM, st>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace bsc

@@ -36,4 +36,27 @@ struct AttnArgs {
 
 cudaError_t launch_attn_fwd(const AttnArgs& args, cudaStream_t st);
 
+// Arguments of the backward kernels (dQ, and dK/dV).
+struct BwdArgs {
+  CUtensorMap tm_q;     // Q bytes, as in AttnArgs
+  CUtensorMap tm_k;     // K bytes, as in AttnArgs
+  CUtensorMap tm_vtn;   // token-normalised V bytes, as in AttnArgs
+  CUtensorMap tm_do;    // dO bf16, 4-D {D, Hq, S, B}, box {64,1,128,1}, 128-byte swizzle
+  const uint8_t* q_sc;
+  const uint8_t* k_sc;
+  const uint8_t* vtn_sc;
+  const void* o;        // bf16 O of the forward, Q's layout
+  const void* dO;       // bf16 dO, Q's layout
+  const float* lse;     // [B][Hq][S], natural log
+  void* dq;             // bf16, Q's layout
+  void* dk;             // bf16, K's layout
+  void* dv;             // bf16, K's layout
+  int32_t* dev_status;
+  unsigned long long limit_ns;
+  int B, S, Hq, Hkv, layout;
+  float scale, scale_log2e;
+};
+
+cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st);
+
 }  // namespace bsc

@@ -161,6 +161,38 @@ typedef struct {
  */
 bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stream);
 
+typedef struct {
+  const uint8_t* q;       /* [in] Q E4M3 bytes, `layout`, Hq heads */
+  const uint8_t* q_sc;    /* [in] Q row atoms */
+  const uint8_t* k;       /* [in] K E4M3 bytes, `layout`, Hkv heads */
+  const uint8_t* k_sc;    /* [in] K row atoms */
+  const uint8_t* vtn;     /* [in] token-normalised V bytes, `layout`, Hkv heads */
+  const uint8_t* vtn_sc;  /* [in] token amplitudes [B][Hkv][S] */
+  const void* o;          /* [in] bf16 O of the forward, `layout`, Hq heads */
+  const float* lse;       /* [in] LSE of the forward, [B][Hq][S], natural log */
+  const void* d_o;        /* [in] bf16 dO, `layout`, Hq heads */
+  void* dq;               /* [out] bf16, `layout`, Hq heads */
+  void* dk;               /* [out] bf16, `layout`, Hkv heads */
+  void* dv;               /* [out] bf16, `layout`, Hkv heads */
+  int B, S, Hq, Hkv, D;
+  int layout;             /* bsc_layout */
+  float softmax_scale;
+  int32_t* dev_status;    /* optional, as in bsc_attn_fwd_params */
+  uint32_t wait_timeout_ms;
+} bsc_attn_bwd_params;
+
+/*
+ * Backward of the leak-free attention on decoded operands ("[PyTorch] Add causal MXFP8 attention
+ * without future-token leakage through V scales", PR #3865, Description, Backward: an FP16/BF16
+ * backward on Q and K decoded from their rowwise MXFP8 bytes and V decoded from the
+ * token-normalised copy, so no gradient depends on a future token).  With s = scale*Qh.Kh^T on
+ * keys j <= i: P = exp(s - LSE), dV = P^T dO, dP = dO.Vt^T, Dlt_i = <dO_i, O_i>,
+ * dS = P*(dP - Dlt), dQ = scale*dS.Kh, dK = scale*dS^T.Qh; GQA: dK, dV of a KV head sum over
+ * the query heads that read it.  BF16 tensor-core MMAs (P and dS rounded to BF16), fp32
+ * accumulation, BF16 outputs.  Uses no memory beyond its arguments.
+ */
+bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream);
+
 /*
  * Synchronises `stream`, reads the int32 at `dev_status` and returns BSC_OK (0) or
  * BSC_ERR_DEVICE_TIMEOUT (non-zero).  The only call that synchronises.
