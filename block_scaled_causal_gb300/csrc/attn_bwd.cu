@@ -13,10 +13,12 @@
 //   * dQ: one CTA per (batch, query head, 128-row query tile); loops over the key tiles up to the
 //     diagonal, accumulating dQ in tensor memory.
 // S = Qh Kh^T is one block-scaled E4M3 MMA on the MXFP8 bytes and scales (exact products); dP, dV,
-// dK and dQ are BF16 MMAs.  Every operand is K-major in shared memory with the 128-byte swizzle;
-// the transposed operands (Q^T, dO^T, K^T, P^T, dS^T) are written there by the threads.  Each
-// iteration runs its phases in turn (loads, decodes, MMAs, elementwise), all threads taking part;
-// thread 0 issues the copies and MMAs.  Every wait is bounded.
+// dK and dQ are BF16 MMAs.  Every tile sits in shared memory in its natural orientation
+// ([row][column], 64-column blocks with the 128-byte swizzle); the products that contract over
+// its rows (P^T dO, dS^T Q, dS K) read it as an MN-major operand, so nothing is transposed.  The
+// next iteration's copies are issued while the current one computes; the phases of an iteration
+// run in turn, all threads taking part, thread 0 issuing the copies and MMAs.  Every wait is
+// bounded.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -32,38 +34,43 @@ constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // keys per tile
 constexpr int HD = 128;   // head dimension
 constexpr int kThreads = 256;
-constexpr uint32_t ATOM = 128 * 128;   // one 128-row x 128-byte swizzle atom column
+constexpr uint32_t ATOM = 128 * 128;   // one 128-row x 128-byte swizzle block (64 BF16 columns)
 
 // TMEM columns: S, dP and two accumulators.  In the dK/dV kernel the scale factors of the S MMA
 // sit at the start of dP's columns; dP is issued only once the S MMA has completed.
 constexpr uint32_t T_S = 0, T_DP = 128, T_ACC0 = 256, T_ACC1 = 384;
 
-enum Bar : uint32_t { B_KV = 0, B_QD, B_MMA1, B_MMA2, B_MMA3, B_DRAIN, B_COUNT };
-enum Site : int { W_KV = 0x20, W_QD, W_MMA1, W_MMA2, W_MMA3 };
+enum Site : int { W_KV = 0x20, W_QD, W_MMA1, W_MMA2, W_MMA3, W_DO };
 
 // A wait's outcome made the same for every thread of the CTA (the TMEM loads are warp-collective).
 __device__ __forceinline__ bool cta_all(bool ok) { return __syncthreads_and(ok ? 1 : 0) != 0; }
 
-// Byte offset of (row, byte column) inside a K-major tile with 128-byte rows, 128-byte swizzle.
+// Byte offset of (row, byte column) inside a tile with 128-byte rows, 128-byte swizzle.
 __device__ __forceinline__ uint32_t sw(uint32_t row, uint32_t colb) {
   return row * 128u + ((((colb >> 4) ^ row) & 7u) << 4) + (colb & 15u);
 }
-// Byte offset of BF16 element (row, col) of a 128-row x 128-column K-major tile (two atoms).
+// Byte offset of BF16 element (row, col) of a 128 x 128 tile (two 64-column blocks).
 __device__ __forceinline__ uint32_t bf_off(uint32_t row, uint32_t col) {
   return (col >> 6) * ATOM + sw(row, (col & 63u) * 2u);
 }
 __device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
   return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);   // 2^(sb-127)
 }
-// E4M3 byte pair -> two floats.
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t pair) {
-  const uint32_t h2 = cvt_e4m3x2_to_f16x2(pair);
-  return make_float2(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))),
-                     __half2float(__ushort_as_half((unsigned short)(h2 >> 16))));
-}
 // Row atom byte of (row, 32-element block) in a 512-byte scale atom.
 __device__ __forceinline__ uint32_t atom_byte(uint32_t row, uint32_t blk) {
   return (row & 31u) * 16u + ((row >> 5) & 3u) * 4u + blk;
+}
+// Eight E4M3 bytes (one uint2) * scale -> eight BF16 (one uint4); exact for in-range values.
+__device__ __forceinline__ uint4 decode8(uint2 bytes, float scale) {
+  const uint32_t bw[2] = {bytes.x, bytes.y};
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t h2 = cvt_e4m3x2_to_f16x2((uint16_t)(bw[e >> 1] >> (16 * (e & 1))));
+    w[e] = pack_bf16x2(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * scale,
+                       __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * scale);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Row statistics of the 128 query rows of tile `it`: LSE in log2 units and Dlt = <dO_i, O_i>.
@@ -95,25 +102,16 @@ __device__ __forceinline__ void row_stats(const BwdArgs& a, int b, int hq, int i
   }
 }
 
-// E4M3 tile [row][d] (TMA, 128-byte swizzle) with row-atom scales -> BF16 transposed [d][row]
-// (K-major with rows = d).  Rows at or past `nrows` become 0.
-__device__ __forceinline__ void decode_transpose(const uint8_t* src8, const uint8_t* sc_atom, uint8_t* dst, int nrows) {
-  for (int unit = threadIdx.x; unit < HD * (BM / 8); unit += kThreads) {
-    const int d = unit & (HD - 1), r0 = (unit >> 7) * 8;
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int ra = r0 + 2 * e, rb = ra + 1;
-      const uint16_t pair = (uint16_t)src8[sw(ra, d)] | ((uint16_t)src8[sw(rb, d)] << 8);
-      const float2 f = e4m3x2_to_f2(pair);
-      const float va = ra < nrows ? f.x * pow2_e8m0(sc_atom[atom_byte(ra, d >> 5)]) : 0.f;
-      const float vb = rb < nrows ? f.y * pow2_e8m0(sc_atom[atom_byte(rb, d >> 5)]) : 0.f;
-      w[e] = pack_bf16x2(va, vb);
-    }
-    *reinterpret_cast<uint4*>(dst + bf_off(d, r0)) = make_uint4(w[0], w[1], w[2], w[3]);
+// E4M3 tile [row][d] (TMA, 128-byte swizzle) with row-atom scales -> BF16 [row][d].  Rows at or
+// past `nrows` become 0.
+__device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* sc_atom, uint8_t* dst, int nrows) {
+  for (int unit = threadIdx.x; unit < BM * (HD / 8); unit += kThreads) {
+    const int r = unit >> 4, d0 = (unit & 15) * 8;
+    const uint2 bytes = *reinterpret_cast<const uint2*>(src8 + sw(r, d0));
+    const float s = r < nrows ? pow2_e8m0(sc_atom[atom_byte(r, d0 >> 5)]) : 0.f;
+    *reinterpret_cast<uint4*>(dst + bf_off(r, d0)) = decode8(bytes, s);
   }
 }
-
 // Token-normalised V bytes [key][d] (TMA, no swizzle) with one amplitude per key -> BF16 [key][d].
 // Keys at or past `nkeys` become 0.
 __device__ __forceinline__ void decode_vt(const uint8_t* raw, const uint8_t* amp, uint8_t* dst, int nkeys) {
@@ -121,40 +119,24 @@ __device__ __forceinline__ void decode_vt(const uint8_t* raw, const uint8_t* amp
     const int key = unit >> 4, d0 = (unit & 15) * 8;
     const uint2 bytes = *reinterpret_cast<const uint2*>(raw + key * HD + d0);
     const float s = key < nkeys ? pow2_e8m0(amp[key]) : 0.f;
-    const uint32_t bw[2] = {bytes.x, bytes.y};
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = e4m3x2_to_f2((uint16_t)(bw[e >> 1] >> (16 * (e & 1))));
-      w[e] = pack_bf16x2(f.x * s, f.y * s);
-    }
-    *reinterpret_cast<uint4*>(dst + bf_off(key, d0)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + bf_off(key, d0)) = decode8(bytes, s);
   }
 }
 
-// BF16 tile [row][d] (two 64-column swizzle atoms) -> transposed [d][row].
-__device__ __forceinline__ void transpose_bf16(const uint8_t* src, uint8_t* dst) {
-  for (int unit = threadIdx.x; unit < HD * (BM / 8); unit += kThreads) {
-    const int d = unit & (HD - 1), r0 = (unit >> 7) * 8;
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t lo = *reinterpret_cast<const uint16_t*>(src + bf_off(r0 + 2 * e, d));
-      const uint32_t hi = *reinterpret_cast<const uint16_t*>(src + bf_off(r0 + 2 * e + 1, d));
-      w[e] = lo | (hi << 16);
-    }
-    *reinterpret_cast<uint4*>(dst + bf_off(d, r0)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-// Sixteen BF16 MMAs of K = 16 over a 128-deep contraction: D (+)= A B^T, A and B K-major tiles of
-// two swizzle atoms each.
+// D (+)= A B^T over a 128-deep contraction in eight BF16 MMAs of K = 16.  A tile read along its
+// columns (K-major) advances 32 bytes per step inside a block; one read along its rows (MN-major,
+// idesc bit 15 for A, 16 for B) advances 16 rows = 2048 bytes, with its two 64-column blocks
+// 16 KB apart.
+template <bool A_MN, bool B_MN>
 __device__ __forceinline__ void mma_bf16_k128(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, bool accumulate) {
+  const uint32_t idesc = idesc_bf16(BM, BN) | (A_MN ? (1u << 15) : 0u) | (B_MN ? (1u << 16) : 0u);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    mma_f16_ss(d_tmem, desc_kmajor_sw128(a_smem + (s >> 2) * ATOM + (s & 3) * 32),
-               desc_kmajor_sw128(b_smem + (s >> 2) * ATOM + (s & 3) * 32), idesc_bf16(BM, BN),
-               (accumulate || s > 0) ? 1u : 0u);
+    const uint64_t da = A_MN ? smem_desc(a_smem + s * 2048, ATOM, 1024, 2)
+                             : desc_kmajor_sw128(a_smem + (s >> 2) * ATOM + (s & 3) * 32);
+    const uint64_t db = B_MN ? smem_desc(b_smem + s * 2048, ATOM, 1024, 2)
+                             : desc_kmajor_sw128(b_smem + (s >> 2) * ATOM + (s & 3) * 32);
+    mma_f16_ss(d_tmem, da, db, idesc, (accumulate || s > 0) ? 1u : 0u);
   }
 }
 // S = Qh Kh^T from E4M3 tiles and row-atom scales (copied to TMEM columns t_sf.. first).
@@ -186,8 +168,8 @@ __device__ __forceinline__ RowView row_view() {
   return v;
 }
 
-// P = exp(s - LSE) of this thread's 64 elements from S in TMEM (row statistics in shared memory);
-// in the diagonal tile keys after the row are masked.
+// P = exp(s - LSE) of this thread's 64 elements from S in TMEM; in the diagonal tile keys after
+// the row are masked.
 __device__ __forceinline__ void compute_p(uint32_t tmem, const RowView& rv, const float* lse2, float sl2, bool diag,
                                           float (&p)[64]) {
   tmem_ld16x256_x16(tmem + T_S + rv.lane_off, p);
@@ -216,6 +198,16 @@ __device__ __forceinline__ void compute_ds(uint32_t tmem, const RowView& rv, con
       ds[4 * k + e] = p[4 * k + e] * (ds[4 * k + e] - da);
       ds[4 * k + 2 + e] = p[4 * k + 2 + e] * (ds[4 * k + 2 + e] - db);
     }
+  }
+}
+// A thread's 64 values as BF16 into a [q][key] tile: keys 8k + 2qd and 8k + 2qd + 1 are adjacent,
+// one 32-bit store per pair.
+__device__ __forceinline__ void store_rows(uint8_t* tile, const RowView& rv, const float (&x)[64]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int key = 8 * k + 2 * rv.qd;
+    *reinterpret_cast<uint32_t*>(tile + bf_off(rv.ra, key)) = pack_bf16x2(x[4 * k], x[4 * k + 1]);
+    *reinterpret_cast<uint32_t*>(tile + bf_off(rv.rb, key)) = pack_bf16x2(x[4 * k + 2], x[4 * k + 3]);
   }
 }
 
@@ -250,22 +242,22 @@ __device__ __forceinline__ void store_acc(uint32_t tmem_acc, void* out, const Bw
 // ================================================================================================
 // dK, dV.  Shared memory (bytes from a 1024-aligned base):
 constexpr uint32_t KV_K8 = 0;                 // K bytes [key][d], swizzled
-constexpr uint32_t KV_VN8 = KV_K8 + 16384;    // token-normalised V bytes [key][d]
-constexpr uint32_t KV_V = KV_VN8 + 16384;     // V bf16 [key][d]
+constexpr uint32_t KV_V = KV_K8 + 16384;      // V bf16 [key][d]
 constexpr uint32_t KV_Q8 = KV_V + 32768;      // Q bytes [q][d], swizzled
-constexpr uint32_t KV_QT = KV_Q8 + 16384;     // Q^T bf16 [d][q]
-constexpr uint32_t KV_DO = KV_QT + 32768;     // dO bf16 [q][d]; then dS^T bf16 [key][q]
-constexpr uint32_t KV_DOT = KV_DO + 32768;    // dO^T bf16 [d][q]
-constexpr uint32_t KV_PT = KV_DOT + 32768;    // P^T bf16 [key][q]
-constexpr uint32_t KV_SFQ = KV_PT + 32768;
+constexpr uint32_t KV_Q = KV_Q8 + 16384;      // Q bf16 [q][d]
+constexpr uint32_t KV_DO = KV_Q + 32768;      // dO bf16 [q][d]
+constexpr uint32_t KV_P = KV_DO + 32768;      // P bf16 [q][key] (the V bytes [key][d] before that)
+constexpr uint32_t KV_VN8 = KV_P;
+constexpr uint32_t KV_DS = KV_P + 32768;      // dS bf16 [q][key]
+constexpr uint32_t KV_SFQ = KV_DS + 32768;
 constexpr uint32_t KV_SFK = KV_SFQ + 512;
 constexpr uint32_t KV_AMP = KV_SFK + 512;
-constexpr uint32_t KV_LSE = KV_AMP + 128;
-constexpr uint32_t KV_DLT = KV_LSE + 512;
-constexpr uint32_t KV_BAR = KV_DLT + 512;
+constexpr uint32_t KV_STAT = KV_AMP + 128;    // [2 buffers][LSE | Dlt][128] floats
+constexpr uint32_t KV_BAR = KV_STAT + 2048;
 constexpr uint32_t KV_MISC = KV_BAR + 64;
 constexpr uint32_t KV_SMEM = KV_MISC + 16 + 1024;
 static_assert(KV_SMEM <= 227 * 1024, "shared memory budget");
+enum KvBar : uint32_t { KB_KV = 0, KB_Q, KB_DO, KB_MMA1, KB_MMA2, KB_MMA3, KB_DRAIN, KB_COUNT };
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -274,8 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   auto bar = [&](uint32_t i) { return sbase + KV_BAR + 8u * i; };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + KV_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_MISC + 4);
-  float* lse2 = reinterpret_cast<float*>(smem + KV_LSE);
-  float* dlt = reinterpret_cast<float*>(smem + KV_DLT);
+  auto stat = [&](int buf) { return reinterpret_cast<float*>(smem + KV_STAT) + buf * 256; };
 
   const int T = (a.S + BN - 1) / BN;
   const int g = a.Hq / a.Hkv;
@@ -285,9 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   const int hk = bh % a.Hkv, b = bh / a.Hkv;
   const long long kv_plane = (long long)b * a.Hkv + hk;
   const int nkeys = min(BN, a.S - jt * BN);
+  const int n_iter = g * (T - jt);   // (query head, query tile) pairs
 
   if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < KB_COUNT; ++i) mbar_init(bar(i), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -301,113 +293,116 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, a.dev_status, a.limit_ns};
   const bool leader = threadIdx.x == 0;
+  auto hq_of = [&](int n) { return hk * g + n / (T - jt); };
+  auto it_of = [&](int n) { return jt + n % (T - jt); };
+  auto load_q = [&](int n) {
+    mbar_arrive_expect_tx(bar(KB_Q), BM * HD + 512);
+    tma_load_4d(sbase + KV_Q8, &a.tm_q, bar(KB_Q), 0, hq_of(n), it_of(n) * BM, b);
+    bulk_load(sbase + KV_SFQ, a.q_sc + (((long long)b * a.Hq + hq_of(n)) * T + it_of(n)) * 512, 512, bar(KB_Q));
+  };
+  auto load_do = [&](int n) {
+    mbar_arrive_expect_tx(bar(KB_DO), 2 * BM * HD);
+    tma_load_4d(sbase + KV_DO, &a.tm_do, bar(KB_DO), 0, hq_of(n), it_of(n) * BM, b);
+    tma_load_4d(sbase + KV_DO + ATOM, &a.tm_do, bar(KB_DO), 64, hq_of(n), it_of(n) * BM, b);
+  };
   bool ok = true;
+  int q_issued = 0, q_seen = 0, do_issued = 0, do_seen = 0;
 
-  // this CTA's K and V tiles
-  const uint32_t namp = (uint32_t)nkeys;
+  // this CTA's K and V tiles, and the first query tile
   if (leader) {
-    mbar_arrive_expect_tx(bar(B_KV), 2 * BN * HD + 512 + namp);
-    tma_load_4d(sbase + KV_K8, &a.tm_k, bar(B_KV), 0, hk, jt * BN, b);
-    bulk_load(sbase + KV_SFK, a.k_sc + (kv_plane * T + jt) * 512, 512, bar(B_KV));
-    tma_load_4d(sbase + KV_VN8, &a.tm_vtn, bar(B_KV), 0, hk, jt * BN, b);
-    bulk_load(sbase + KV_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, namp, bar(B_KV));
+    mbar_arrive_expect_tx(bar(KB_KV), 2 * BN * HD + 512 + (uint32_t)nkeys);
+    tma_load_4d(sbase + KV_K8, &a.tm_k, bar(KB_KV), 0, hk, jt * BN, b);
+    bulk_load(sbase + KV_SFK, a.k_sc + (kv_plane * T + jt) * 512, 512, bar(KB_KV));
+    tma_load_4d(sbase + KV_VN8, &a.tm_vtn, bar(KB_KV), 0, hk, jt * BN, b);
+    bulk_load(sbase + KV_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, (uint32_t)nkeys, bar(KB_KV));
+    load_q(0);
+    load_do(0);
   }
-  ok = cta_all(mbar_wait(bar(B_KV), 0, ctl, W_KV));
-  bool kv_seen = ok;
+  q_issued = do_issued = 1;
+  row_stats(a, b, hq_of(0), it_of(0), stat(0), stat(0) + 128);
+  ok = cta_all(mbar_wait(bar(KB_KV), 0, ctl, W_KV));
+  const bool kv_seen = ok;
   if (ok) decode_vt(smem + KV_VN8, smem + KV_AMP, smem + KV_V, nkeys);
+  __syncthreads();   // the V bytes are read before P overwrites them
 
   const RowView rv = row_view();
-  int iter = 0, qd_issued = 0, qd_seen = 0;
-  for (int hq = hk * g; hq < hk * g + g; ++hq) {
-    for (int it = jt; it < T; ++it, ++iter) {
-      const uint32_t par = (uint32_t)iter & 1u;
-      if (leader && ok) {
-        mbar_arrive_expect_tx(bar(B_QD), BM * HD + 512 + 2 * BM * HD);
-        tma_load_4d(sbase + KV_Q8, &a.tm_q, bar(B_QD), 0, hq, it * BM, b);
-        bulk_load(sbase + KV_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + it) * 512, 512, bar(B_QD));
-        tma_load_4d(sbase + KV_DO, &a.tm_do, bar(B_QD), 0, hq, it * BM, b);
-        tma_load_4d(sbase + KV_DO + ATOM, &a.tm_do, bar(B_QD), 64, hq, it * BM, b);
+  for (int n = 0; n < n_iter; ++n) {
+    const uint32_t par = (uint32_t)n & 1u;
+    const int it = it_of(n);
+    float* lse2 = stat(n & 1);
+    float* dlt = lse2 + 128;
+    if (ok) ok = mbar_wait(bar(KB_Q), par, ctl, W_QD);
+    ok = cta_all(ok);
+    if (ok) ++q_seen;
+    if (ok) decode_rows(smem + KV_Q8, smem + KV_SFQ, smem + KV_Q, min(BM, a.S - it * BM));
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // S first: its scale factors occupy dP's first columns until it has completed
+    if (leader && ok) {
+      mma_s(tmem, T_DP, sbase + KV_Q8, sbase + KV_K8, sbase + KV_SFQ, sbase + KV_SFK);
+      tc_commit(bar(KB_MMA1));
+    }
+    if (ok) ok = mbar_wait(bar(KB_MMA1), par, ctl, W_MMA1);
+    ok = cta_all(ok);
+    tc_fence_after();
+    if (ok) ok = mbar_wait(bar(KB_DO), par, ctl, W_DO);
+    ok = cta_all(ok);
+    if (ok) ++do_seen;
+    if (leader && ok) {
+      if (n + 1 < n_iter) {   // the Q bytes are free again: fetch the next query tile's
+        load_q(n + 1);
+        ++q_issued;
       }
-      if (ok) ++qd_issued;
-      row_stats(a, b, hq, it, lse2, dlt);
-      if (ok) ok = mbar_wait(bar(B_QD), par, ctl, W_QD);
-      ok = cta_all(ok);
-      if (ok) ++qd_seen;
-      if (ok) {
-        decode_transpose(smem + KV_Q8, smem + KV_SFQ, smem + KV_QT, min(BM, a.S - it * BM));
-        transpose_bf16(smem + KV_DO, smem + KV_DOT);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      // S first: its scale factors occupy dP's first columns until it has completed
-      if (leader && ok) {
-        mma_s(tmem, T_DP, sbase + KV_Q8, sbase + KV_K8, sbase + KV_SFQ, sbase + KV_SFK);
-        tc_commit(bar(B_MMA1));
-      }
-      if (ok) ok = mbar_wait(bar(B_MMA1), par, ctl, W_MMA1);
-      ok = cta_all(ok);
-      tc_fence_after();
-      if (leader && ok) {
-        mma_bf16_k128(tmem + T_DP, sbase + KV_DO, sbase + KV_V, false);   // dP = dO V^T
-        tc_commit(bar(B_MMA3));
-      }
-      float p[64];
-      if (ok) {
-        compute_p(tmem, rv, lse2, a.scale_log2e, it == jt, p);
-        uint8_t* pt = smem + KV_PT;   // P^T [key][q]
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = 8 * k + 2 * rv.qd + e;
-            *reinterpret_cast<__nv_bfloat16*>(pt + bf_off(key, rv.ra)) = __float2bfloat16_rn(p[4 * k + e]);
-            *reinterpret_cast<__nv_bfloat16*>(pt + bf_off(key, rv.rb)) = __float2bfloat16_rn(p[4 * k + 2 + e]);
-          }
-        }
-      }
-      if (ok) ok = mbar_wait(bar(B_MMA3), par, ctl, W_MMA3);
-      ok = cta_all(ok);
-      tc_fence_after();
-      if (ok) {
-        float ds[64];
-        compute_ds(tmem, rv, dlt, p, ds);
-        uint8_t* dst = smem + KV_DO;   // dS^T [key][q] over dO, which the dP MMA has read
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = 8 * k + 2 * rv.qd + e;
-            *reinterpret_cast<__nv_bfloat16*>(dst + bf_off(key, rv.ra)) = __float2bfloat16_rn(ds[4 * k + e]);
-            *reinterpret_cast<__nv_bfloat16*>(dst + bf_off(key, rv.rb)) = __float2bfloat16_rn(ds[4 * k + 2 + e]);
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (leader && ok) {
-        mma_bf16_k128(tmem + T_ACC0, sbase + KV_PT, sbase + KV_DOT, iter > 0);   // dV += P^T dO
-        mma_bf16_k128(tmem + T_ACC1, sbase + KV_DO, sbase + KV_QT, iter > 0);    // dK += dS^T Q
-        tc_commit(bar(B_MMA2));
-      }
-      if (ok) ok = mbar_wait(bar(B_MMA2), par, ctl, W_MMA2);
-      ok = cta_all(ok);
-      tc_fence_after();
+      mma_bf16_k128<false, false>(tmem + T_DP, sbase + KV_DO, sbase + KV_V, false);   // dP = dO V^T
+      tc_commit(bar(KB_MMA3));
+    }
+    float p[64];
+    if (ok) {
+      compute_p(tmem, rv, lse2, a.scale_log2e, it == jt, p);
+      store_rows(smem + KV_P, rv, p);
+    }
+    if (n + 1 < n_iter) {
+      float* nx = stat((n + 1) & 1);
+      row_stats(a, b, hq_of(n + 1), it_of(n + 1), nx, nx + 128);
+    }
+    if (ok) ok = mbar_wait(bar(KB_MMA3), par, ctl, W_MMA3);
+    ok = cta_all(ok);
+    tc_fence_after();
+    if (ok) {
+      float ds[64];
+      compute_ds(tmem, rv, dlt, p, ds);
+      store_rows(smem + KV_DS, rv, ds);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (leader && ok) {
+      mma_bf16_k128<true, true>(tmem + T_ACC0, sbase + KV_P, sbase + KV_DO, n > 0);   // dV += P^T dO
+      mma_bf16_k128<true, true>(tmem + T_ACC1, sbase + KV_DS, sbase + KV_Q, n > 0);   // dK += dS^T Q
+      tc_commit(bar(KB_MMA2));
+    }
+    if (ok) ok = mbar_wait(bar(KB_MMA2), par, ctl, W_MMA2);
+    ok = cta_all(ok);
+    tc_fence_after();
+    if (leader && ok && n + 1 < n_iter) {   // dO is free again
+      load_do(n + 1);
+      ++do_issued;
     }
   }
-  if (ok && iter > 0) {
+  if (ok && n_iter > 0) {
     store_acc(tmem + T_ACC0, a.dv, a, a.Hkv, b, hk, jt, 1.0f);
     store_acc(tmem + T_ACC1, a.dk, a, a.Hkv, b, hk, jt, a.scale);
   }
   if (leader) {
     // every tcgen05 operation and copy this thread issued must finish before the CTA exits
-    tc_commit(bar(B_DRAIN));
-    mbar_wait_drain(bar(B_DRAIN), 0, a.limit_ns);
-    if (!kv_seen) mbar_wait_drain(bar(B_KV), 0, a.limit_ns);
-    if (qd_issued > qd_seen) mbar_wait_drain(bar(B_QD), (uint32_t)(qd_issued - 1) & 1u, a.limit_ns);
+    tc_commit(bar(KB_DRAIN));
+    mbar_wait_drain(bar(KB_DRAIN), 0, a.limit_ns);
+    if (!kv_seen) mbar_wait_drain(bar(KB_KV), 0, a.limit_ns);
+    if (q_issued > q_seen) mbar_wait_drain(bar(KB_Q), (uint32_t)(q_issued - 1) & 1u, a.limit_ns);
+    if (do_issued > do_seen) mbar_wait_drain(bar(KB_DO), (uint32_t)(do_issued - 1) & 1u, a.limit_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -417,22 +412,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 
 // ================================================================================================
 // dQ.  Shared memory:
-constexpr uint32_t QQ_Q8 = 0;                 // Q bytes [q][d], swizzled
-constexpr uint32_t QQ_DO = QQ_Q8 + 16384;     // dO bf16 [q][d]
-constexpr uint32_t QQ_K8 = QQ_DO + 32768;     // K bytes [key][d], swizzled
-constexpr uint32_t QQ_VN8 = QQ_K8 + 16384;    // token-normalised V bytes [key][d]
-constexpr uint32_t QQ_KT = QQ_VN8 + 16384;    // K^T bf16 [d][key]
-constexpr uint32_t QQ_V = QQ_KT + 32768;      // V bf16 [key][d]
-constexpr uint32_t QQ_DS = QQ_V + 32768;      // dS bf16 [q][key]
+constexpr uint32_t QQ_Q8 = 0;                       // Q bytes [q][d], swizzled
+constexpr uint32_t QQ_DO = QQ_Q8 + 16384;           // dO bf16 [q][d]
+constexpr uint32_t QQ_K8 = QQ_DO + 32768;           // 2 stages: K bytes [key][d], swizzled
+constexpr uint32_t QQ_VN8 = QQ_K8 + 2 * 16384;      // 2 stages: token-normalised V bytes [key][d]
+constexpr uint32_t QQ_K = QQ_VN8 + 2 * 16384;       // K bf16 [key][d]
+constexpr uint32_t QQ_V = QQ_K + 32768;             // V bf16 [key][d]
+constexpr uint32_t QQ_DS = QQ_V + 32768;            // dS bf16 [q][key]
 constexpr uint32_t QQ_SFQ = QQ_DS + 32768;
-constexpr uint32_t QQ_SFK = QQ_SFQ + 512;
-constexpr uint32_t QQ_AMP = QQ_SFK + 512;
-constexpr uint32_t QQ_LSE = QQ_AMP + 128;
+constexpr uint32_t QQ_SFK = QQ_SFQ + 512;           // 2 stages
+constexpr uint32_t QQ_AMP = QQ_SFK + 1024;          // 2 stages of 128
+constexpr uint32_t QQ_LSE = QQ_AMP + 256;
 constexpr uint32_t QQ_DLT = QQ_LSE + 512;
 constexpr uint32_t QQ_BAR = QQ_DLT + 512;
 constexpr uint32_t QQ_MISC = QQ_BAR + 64;
 constexpr uint32_t QQ_SMEM = QQ_MISC + 16 + 1024;
 static_assert(QQ_SMEM <= 227 * 1024, "shared memory budget");
+enum QBar : uint32_t { QB_QD = 0, QB_KV0, QB_KV1, QB_MMA1, QB_MMA2, QB_DRAIN, QB_COUNT };
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -452,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   const long long kv_plane = (long long)b * a.Hkv + hk;
 
   if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < QB_COUNT; ++i) mbar_init(bar(i), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -466,82 +462,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, a.dev_status, a.limit_ns};
   const bool leader = threadIdx.x == 0;
+  // key tile j into stage j % 2
+  auto load_kv = [&](int j) {
+    const int st = j & 1;
+    const uint32_t nk = (uint32_t)min(BN, a.S - j * BN);
+    const uint32_t kb = bar(QB_KV0 + st);
+    mbar_arrive_expect_tx(kb, 2 * BN * HD + 512 + nk);
+    tma_load_4d(sbase + QQ_K8 + st * 16384, &a.tm_k, kb, 0, hk, j * BN, b);
+    bulk_load(sbase + QQ_SFK + st * 512, a.k_sc + (kv_plane * T + j) * 512, 512, kb);
+    tma_load_4d(sbase + QQ_VN8 + st * 16384, &a.tm_vtn, kb, 0, hk, j * BN, b);
+    bulk_load(sbase + QQ_AMP + st * 128, a.vtn_sc + kv_plane * a.S + (long long)j * BN, nk, kb);
+  };
   bool ok = true;
+  int kv_issued[2] = {0, 0}, kv_seen[2] = {0, 0};
 
   if (leader) {
-    mbar_arrive_expect_tx(bar(B_QD), BM * HD + 512 + 2 * BM * HD);
-    tma_load_4d(sbase + QQ_Q8, &a.tm_q, bar(B_QD), 0, hq, it * BM, b);
-    bulk_load(sbase + QQ_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + it) * 512, 512, bar(B_QD));
-    tma_load_4d(sbase + QQ_DO, &a.tm_do, bar(B_QD), 0, hq, it * BM, b);
-    tma_load_4d(sbase + QQ_DO + ATOM, &a.tm_do, bar(B_QD), 64, hq, it * BM, b);
+    mbar_arrive_expect_tx(bar(QB_QD), BM * HD + 512 + 2 * BM * HD);
+    tma_load_4d(sbase + QQ_Q8, &a.tm_q, bar(QB_QD), 0, hq, it * BM, b);
+    bulk_load(sbase + QQ_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + it) * 512, 512, bar(QB_QD));
+    tma_load_4d(sbase + QQ_DO, &a.tm_do, bar(QB_QD), 0, hq, it * BM, b);
+    tma_load_4d(sbase + QQ_DO + ATOM, &a.tm_do, bar(QB_QD), 64, hq, it * BM, b);
+    load_kv(0);
   }
+  kv_issued[0] = 1;
   row_stats(a, b, hq, it, lse2, dlt);
-  ok = cta_all(mbar_wait(bar(B_QD), 0, ctl, W_QD));
+  ok = cta_all(mbar_wait(bar(QB_QD), 0, ctl, W_QD));
   const bool qd_seen = ok;
 
   const RowView rv = row_view();
-  int kv_issued = 0, kv_seen = 0;
   for (int jt = 0; jt <= it; ++jt) {
     const uint32_t par = (uint32_t)jt & 1u;
+    const int st = jt & 1;
     const int nkeys = min(BN, a.S - jt * BN);
-    if (leader && ok) {
-      mbar_arrive_expect_tx(bar(B_KV), 2 * BN * HD + 512 + (uint32_t)nkeys);
-      tma_load_4d(sbase + QQ_K8, &a.tm_k, bar(B_KV), 0, hk, jt * BN, b);
-      bulk_load(sbase + QQ_SFK, a.k_sc + (kv_plane * T + jt) * 512, 512, bar(B_KV));
-      tma_load_4d(sbase + QQ_VN8, &a.tm_vtn, bar(B_KV), 0, hk, jt * BN, b);
-      bulk_load(sbase + QQ_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, (uint32_t)nkeys, bar(B_KV));
-    }
-    if (ok) ++kv_issued;
-    if (ok) ok = mbar_wait(bar(B_KV), par, ctl, W_KV);
+    if (leader && ok && jt + 1 <= it) load_kv(jt + 1);   // stage st^1 was last read in iteration jt-1
+    if (ok && jt + 1 <= it) ++kv_issued[st ^ 1];
+    if (ok) ok = mbar_wait(bar(QB_KV0 + st), (uint32_t)(jt >> 1) & 1u, ctl, W_KV);
     ok = cta_all(ok);
-    if (ok) ++kv_seen;
+    if (ok) ++kv_seen[st];
     if (ok) {
-      decode_vt(smem + QQ_VN8, smem + QQ_AMP, smem + QQ_V, nkeys);
-      decode_transpose(smem + QQ_K8, smem + QQ_SFK, smem + QQ_KT, nkeys);
+      decode_vt(smem + QQ_VN8 + st * 16384, smem + QQ_AMP + st * 128, smem + QQ_V, nkeys);
+      decode_rows(smem + QQ_K8 + st * 16384, smem + QQ_SFK + st * 512, smem + QQ_K, nkeys);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (leader && ok) {
-      mma_s(tmem, T_ACC1, sbase + QQ_Q8, sbase + QQ_K8, sbase + QQ_SFQ, sbase + QQ_SFK);
-      mma_bf16_k128(tmem + T_DP, sbase + QQ_DO, sbase + QQ_V, false);   // dP = dO V^T
-      tc_commit(bar(B_MMA1));
+      mma_s(tmem, T_ACC1, sbase + QQ_Q8, sbase + QQ_K8 + st * 16384, sbase + QQ_SFQ, sbase + QQ_SFK + st * 512);
+      mma_bf16_k128<false, false>(tmem + T_DP, sbase + QQ_DO, sbase + QQ_V, false);   // dP = dO V^T
+      tc_commit(bar(QB_MMA1));
     }
-    if (ok) ok = mbar_wait(bar(B_MMA1), par, ctl, W_MMA1);
+    if (ok) ok = mbar_wait(bar(QB_MMA1), par, ctl, W_MMA1);
     ok = cta_all(ok);
     tc_fence_after();
     if (ok) {
       float p[64], ds[64];
       compute_p(tmem, rv, lse2, a.scale_log2e, jt == it, p);
       compute_ds(tmem, rv, dlt, p, ds);
-      // dS [q][key]: keys 8k + 2qd and 8k + 2qd + 1 are adjacent, one 32-bit store per pair
-      uint8_t* dsm = smem + QQ_DS;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int key = 8 * k + 2 * rv.qd;
-        *reinterpret_cast<uint32_t*>(dsm + bf_off(rv.ra, key)) = pack_bf16x2(ds[4 * k], ds[4 * k + 1]);
-        *reinterpret_cast<uint32_t*>(dsm + bf_off(rv.rb, key)) = pack_bf16x2(ds[4 * k + 2], ds[4 * k + 3]);
-      }
+      store_rows(smem + QQ_DS, rv, ds);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (leader && ok) {
-      mma_bf16_k128(tmem + T_ACC0, sbase + QQ_DS, sbase + QQ_KT, jt > 0);   // dQ += dS K
-      tc_commit(bar(B_MMA2));
+      mma_bf16_k128<false, true>(tmem + T_ACC0, sbase + QQ_DS, sbase + QQ_K, jt > 0);   // dQ += dS K
+      tc_commit(bar(QB_MMA2));
     }
-    if (ok) ok = mbar_wait(bar(B_MMA2), par, ctl, W_MMA2);
+    if (ok) ok = mbar_wait(bar(QB_MMA2), par, ctl, W_MMA2);
     ok = cta_all(ok);
     tc_fence_after();
   }
   if (ok) store_acc(tmem + T_ACC0, a.dq, a, a.Hq, b, hq, it, a.scale);
   if (leader) {
-    tc_commit(bar(B_DRAIN));
-    mbar_wait_drain(bar(B_DRAIN), 0, a.limit_ns);
-    if (!qd_seen) mbar_wait_drain(bar(B_QD), 0, a.limit_ns);
-    if (kv_issued > kv_seen) mbar_wait_drain(bar(B_KV), (uint32_t)(kv_issued - 1) & 1u, a.limit_ns);
+    tc_commit(bar(QB_DRAIN));
+    mbar_wait_drain(bar(QB_DRAIN), 0, a.limit_ns);
+    if (!qd_seen) mbar_wait_drain(bar(QB_QD), 0, a.limit_ns);
+    for (int s2 = 0; s2 < 2; ++s2)
+      if (kv_issued[s2] > kv_seen[s2]) mbar_wait_drain(bar(QB_KV0 + s2), (uint32_t)(kv_issued[s2] - 1) & 1u, a.limit_ns);
   }
   tc_fence_before();
   __syncthreads();
