@@ -30,6 +30,11 @@ What it follows
   A block holding a NaN or an infinity gets scale byte 0xFF and element bytes
   0x7F (the E8M0 and E4M3 NaN codes).
 
+  A second scale rule, "ceil", rounds the scale up instead so that no element saturates:
+  e = ceil(log2(amax / 448)), the smallest e with amax * 2^-e <= 448.  The pages note that TE's
+  own quantisation kernels, not the OCP text, chose its scales; covering the block maximum is the
+  plain reading of that.  Everything else is unchanged.
+
 Everything is fp64 numpy.  Element values are returned as float64 arrays;
 bytes as uint8 arrays.
 """
@@ -97,10 +102,20 @@ def e4m3_decode(b: np.ndarray) -> np.ndarray:
     return s * val
 
 
-def e8m0_exponent(amax: np.ndarray) -> np.ndarray:
-    """Shared exponent e (scale = 2**e) for finite block maxima, OCP MX rule for E4M3 elements."""
+def e8m0_exponent(amax: np.ndarray, rule: str = "floor") -> np.ndarray:
+    """Shared exponent e (scale = 2**e) for finite block maxima.
+
+    rule "floor": the OCP MX rule for E4M3 elements, floor(log2 amax) - 8.
+    rule "ceil": ceil(log2(amax / 448)): one more than "floor" exactly when amax exceeds
+    448 * 2**("floor" exponent), i.e. when the significand of amax is above 1.75.
+    """
     amax = np.asarray(amax, dtype=np.float64)
-    e = _floor_log2(np.where(amax > 0, amax, 1.0)) - E4M3_EMAX
+    fl = _floor_log2(np.where(amax > 0, amax, 1.0))
+    e = fl - E4M3_EMAX
+    if rule == "ceil":
+        e = e + (np.where(amax > 0, amax, 1.0) > np.ldexp(E4M3_MAX / 256.0, fl)).astype(np.int64)
+    elif rule != "floor":
+        raise ValueError(rule)
     e = np.where(amax > 0, e, -E8M0_BIAS)
     return np.clip(e, -E8M0_BIAS, E8M0_BIAS)
 
@@ -111,8 +126,9 @@ def e8m0_decode(sb: np.ndarray) -> np.ndarray:
     return np.where(sb == 0xFF, np.nan, np.ldexp(1.0, sb - E8M0_BIAS))
 
 
-def mx_quantize(x: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
-    """Quantise along the LAST axis in blocks of k consecutive elements.
+def mx_quantize(x: np.ndarray, k: int, rule: str = "floor") -> tuple[np.ndarray, np.ndarray]:
+    """Quantise along the LAST axis in blocks of k consecutive elements (scale rule as in
+    e8m0_exponent).
 
     Returns (element bytes with x's shape, scale bytes with shape x.shape[:-1] + (n/k,)).
     """
@@ -123,7 +139,7 @@ def mx_quantize(x: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
     xb = x.reshape(x.shape[:-1] + (n // k, k))
     finite = np.all(np.isfinite(xb), axis=-1)
     amax = np.max(np.abs(np.where(np.isfinite(xb), xb, 0.0)), axis=-1)
-    e = e8m0_exponent(amax)
+    e = e8m0_exponent(amax, rule)
     y = np.ldexp(xb, -e[..., None])            # x * 2**-e, exact
     q = e4m3_round(np.where(np.isfinite(y), y, 0.0))
     codes = e4m3_encode(q)
@@ -147,12 +163,12 @@ def mx_dequantize(codes: np.ndarray, sbytes: np.ndarray, k: int) -> np.ndarray:
 MX_BLOCK = 32
 
 
-def quantize_rowwise(x: np.ndarray):
+def quantize_rowwise(x: np.ndarray, rule: str = "floor"):
     """Q or K: one scale per 32 consecutive head-dim elements of each (b, s, h) row.
 
     Returns (bytes [B,S,H,D], scales [B,H,S,D/32]).
     """
-    codes, sb = mx_quantize(x, MX_BLOCK)                 # sb: [B,S,H,D/32]
+    codes, sb = mx_quantize(x, MX_BLOCK, rule)           # sb: [B,S,H,D/32]
     return codes, np.ascontiguousarray(sb.transpose(0, 2, 1, 3))
 
 
@@ -160,13 +176,13 @@ def dequantize_rowwise(codes: np.ndarray, sc: np.ndarray) -> np.ndarray:
     return mx_dequantize(codes, np.ascontiguousarray(sc.transpose(0, 2, 1, 3)), MX_BLOCK)
 
 
-def quantize_colwise(v: np.ndarray):
+def quantize_colwise(v: np.ndarray, rule: str = "floor"):
     """V columnwise: one scale per 32 consecutive tokens of each (b, h, d) column.
 
     Returns (bytes of V transposed to [B,H,D,S], scales [B,H,D,S/32]).
     """
     vt = np.ascontiguousarray(np.asarray(v, dtype=np.float64).transpose(0, 2, 3, 1))  # [B,H,D,S]
-    return mx_quantize(vt, MX_BLOCK)
+    return mx_quantize(vt, MX_BLOCK, rule)
 
 
 def dequantize_colwise(codes_t: np.ndarray, sc: np.ndarray) -> np.ndarray:
@@ -174,7 +190,7 @@ def dequantize_colwise(codes_t: np.ndarray, sc: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(mx_dequantize(codes_t, sc, MX_BLOCK).transpose(0, 3, 1, 2))
 
 
-def quantize_token_norm(v: np.ndarray):
+def quantize_token_norm(v: np.ndarray, rule: str = "floor"):
     """Token-normalised V: one power-of-two amplitude per (b, s, h) token row of D elements.
 
     The pages fix only "one power-of-two amplitude per token"; the amplitude is chosen by the
@@ -182,7 +198,7 @@ def quantize_token_norm(v: np.ndarray):
     Returns (bytes [B,S,H,D], scales [B,H,S]).
     """
     v = np.asarray(v, dtype=np.float64)
-    codes, sb = mx_quantize(v, v.shape[-1])              # sb: [B,S,H,1]
+    codes, sb = mx_quantize(v, v.shape[-1], rule)        # sb: [B,S,H,1]
     return codes, np.ascontiguousarray(sb[..., 0].transpose(0, 2, 1))
 
 

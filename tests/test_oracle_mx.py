@@ -204,3 +204,48 @@ def test_block_locality():
     assert [tuple(d) for d in diff_blocks] == [(2, 2)]
     mask = np.ones_like(c0, dtype=bool); mask[2, 64:96] = False
     np.testing.assert_array_equal(c0[mask], c1[mask])
+
+
+# ----------------------------------------------------------------------------------------------
+# The "ceil" scale rule (the scale rounded up so that no element saturates).
+
+def test_ceil_rule_worked_example_saturation_block():
+    """amax = 3.75: floor rule e = -7 (byte 0x78) saturates 480 to 448 (0x7E); ceil rule e = -6
+    (byte 0x79), 3.75 * 64 = 240 = 1.875 * 2^7 exactly, byte 0x77."""
+    x = np.array([[3.75] + [0.0] * 31])
+    c_f, s_f = mx.mx_quantize(x, 32, "floor")
+    c_c, s_c = mx.mx_quantize(x, 32, "ceil")
+    assert s_f[0, 0] == 0x78 and c_f[0, 0] == 0x7E
+    assert s_c[0, 0] == 0x79 and c_c[0, 0] == 0x77
+    assert mx.mx_dequantize(c_c, s_c, 32)[0, 0] == 3.75
+
+
+def test_ceil_rule_is_the_smallest_non_saturating_scale():
+    """Brute force: for random block maxima, e_ceil is the smallest e with amax * 2^-e <= 448, and
+    it equals the floor-rule exponent or one more."""
+    rng = np.random.default_rng(7)
+    amax = np.ldexp(rng.uniform(1.0, 2.0, 4000), rng.integers(-60, 60, 4000))
+    amax = np.concatenate([amax, np.ldexp(1.75, np.arange(-20, 20)), np.ldexp(np.nextafter(1.75, 2), np.arange(-20, 20))])
+    e = mx.e8m0_exponent(amax, "ceil")
+    ef = mx.e8m0_exponent(amax, "floor")
+    assert np.all(np.ldexp(amax, -e) <= 448.0)
+    assert np.all(np.ldexp(amax, -(e - 1)) > 448.0)
+    assert np.all((e == ef) | (e == ef + 1))
+    # significand exactly 1.75 keeps the floor exponent (amax * 2^-e = 448 exactly)
+    at = np.ldexp(1.75, np.arange(-20, 20))
+    np.testing.assert_array_equal(mx.e8m0_exponent(at, "ceil"), mx.e8m0_exponent(at, "floor"))
+
+
+def test_ceil_rule_never_saturates_and_matches_floor_elsewhere():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((64, 128)) * np.exp(rng.uniform(-8, 8, (64, 1)))
+    cc, sc = mx.mx_quantize(x, 32, "ceil")
+    cf, sf = mx.mx_quantize(x, 32, "floor")
+    dec = mx.mx_dequantize(cc, sc, 32)
+    # no element at the saturation code unless it is exactly 448 * 2^e
+    y = np.ldexp(x.reshape(64, 4, 32), -(sc.astype(np.int64) - 127)[..., None]).reshape(64, 128)
+    assert np.all(np.abs(y) <= 448.0)
+    same = (sc == sf)
+    np.testing.assert_array_equal(cc.reshape(64, 4, 32)[same], cf.reshape(64, 4, 32)[same])
+    assert np.all(np.abs(dec - x) <= np.ldexp(1.0, (np.floor(np.log2(np.maximum(np.abs(x), 1e-300))) - 4).astype(np.int64))
+                  + np.ldexp(1.0, (sc.astype(np.int64) - 127 - 10)).repeat(32, axis=1))
