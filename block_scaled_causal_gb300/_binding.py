@@ -37,6 +37,8 @@ def _load():
     lib.mxfp8_quantize_v_fused.argtypes = [vp, i32, i32, i32, i32, i32, u8p, u8p, u8p, u8p, vp]
     lib.mxfp8_causal_attn_fwd.restype = i32
     lib.mxfp8_causal_attn_fwd.argtypes = [ctypes.POINTER(AttnFwdParams), vp]
+    lib.mxfp8_quantize.restype = i32
+    lib.mxfp8_quantize.argtypes = [ctypes.POINTER(QuantParams), vp]
     lib.bf16_attn_bwd.restype = i32
     lib.bf16_attn_bwd.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
     lib.bsc_read_device_status.restype = i32
@@ -59,6 +61,21 @@ class AttnFwdParams(ctypes.Structure):
         ("debug_stall", ctypes.c_int),
         ("o_e4m3", ctypes.c_void_p), ("o_sc", ctypes.c_void_p),
     ]
+
+
+class QuantParams(ctypes.Structure):
+    """Mirror of bsc_quant_params."""
+    _fields_ = [
+        ("kind", ctypes.c_int), ("x", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("S", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int),
+        ("layout", ctypes.c_int), ("rule", ctypes.c_int),
+        ("e4m3", ctypes.c_void_p), ("sc", ctypes.c_void_p),
+        ("vtn_e4m3", ctypes.c_void_p), ("vtn_sc", ctypes.c_void_p),
+    ]
+
+
+QUANT_ROWWISE, QUANT_V_COLWISE, QUANT_V_TOKEN_NORM, QUANT_V_FUSED = 0, 1, 2, 3
+SCALE_FLOOR, SCALE_CEIL = 0, 1
 
 
 class AttnBwdParams(ctypes.Structure):
@@ -258,3 +275,28 @@ def forward_backward(q, k, v, do, layout=BSHD, softmax_scale=None, stream=None):
     o, lse = mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, stream=stream)
     dq, dk, dv = bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o, lse, do, layout, softmax_scale, stream=stream)
     return o, lse, dq, dk, dv
+
+
+def mxfp8_quantize(kind, x, layout=BSHD, rule=SCALE_FLOOR, stream=None):
+    """Any quantisation with a chosen scale rule.  Returns the outputs of the matching call:
+    (bytes, row atoms) for QUANT_ROWWISE, (V^T bytes, column atoms) for QUANT_V_COLWISE,
+    (token-normalised bytes, amplitudes) for QUANT_V_TOKEN_NORM, all four for QUANT_V_FUSED."""
+    _require(x, torch.bfloat16, "x")
+    B, S, H, D = _bshd_dims(x, layout)
+    T = (S + 127) // 128
+    u8 = dict(dtype=torch.uint8, device=x.device)
+    e4m3 = sc = vtn = vtn_sc = None
+    if kind == QUANT_ROWWISE:
+        e4m3, sc = torch.empty(x.shape, **u8), torch.empty((B, H, T, 512), **u8)
+    if kind in (QUANT_V_COLWISE, QUANT_V_FUSED):
+        e4m3, sc = torch.empty((B, H, D, S), **u8), torch.empty((B, H, T, 512), **u8)
+    if kind in (QUANT_V_TOKEN_NORM, QUANT_V_FUSED):
+        vtn, vtn_sc = torch.empty(x.shape, **u8), torch.empty((B, H, S), **u8)
+    p = QuantParams(kind=kind, x=x.data_ptr(), B=B, S=S, H=H, D=D, layout=layout, rule=rule,
+                    e4m3=_ptr(e4m3), sc=_ptr(sc), vtn_e4m3=_ptr(vtn), vtn_sc=_ptr(vtn_sc))
+    _check(lib.mxfp8_quantize(ctypes.byref(p), _stream(stream)))
+    if kind == QUANT_V_FUSED:
+        return e4m3, sc, vtn, vtn_sc
+    if kind == QUANT_V_TOKEN_NORM:
+        return vtn, vtn_sc
+    return e4m3, sc

@@ -111,7 +111,8 @@ bool encode_vt_map(CUtensorMap* m, const void* base, long long rows, int S) {
 bsc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BSC_OK : BSC_ERR_CUDA; }
 
 bsc_status quant_v_common(const void* v, int B, int S, int H, int D, bsc_layout layout, uint8_t* vt, uint8_t* vsc,
-                          uint8_t* vtn, uint8_t* vtn_sc, bsc_stream_t stream, bool want_col, bool want_tn) {
+                          uint8_t* vtn, uint8_t* vtn_sc, bsc_stream_t stream, bool want_col, bool want_tn,
+                          int rule = 0) {
   bool empty;
   bsc_status s = check_shape(B, S, H, D, layout, &empty);
   if (s != BSC_OK || empty) return s;
@@ -122,7 +123,7 @@ bsc_status quant_v_common(const void* v, int B, int S, int H, int D, bsc_layout 
   if ((s = check_device()) != BSC_OK) return s;
   return from_cuda(bsc::launch_quant_v(v, want_col ? vt : nullptr, want_col ? vsc : nullptr,
                                        want_tn ? vtn : nullptr, want_tn ? vtn_sc : nullptr, B, S, H, layout,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+                                       reinterpret_cast<cudaStream_t>(stream), rule));
 }
 
 }  // namespace
@@ -153,6 +154,35 @@ bsc_status mxfp8_quantize_qk_rowwise(const void* x, int B, int S, int H, int D, 
   if (!aligned16(x) || !aligned16(xq) || !aligned16(xsc)) return BSC_ERR_ALIGN;
   if ((s = check_device()) != BSC_OK) return s;
   return from_cuda(bsc::launch_quant_rowwise(x, xq, xsc, B, S, H, layout, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bsc_status mxfp8_quantize(const bsc_quant_params* p, bsc_stream_t stream) {
+  if (!p) return BSC_ERR_NULL;
+  if (p->rule != BSC_SCALE_FLOOR && p->rule != BSC_SCALE_CEIL) return BSC_ERR_UNSUPPORTED;
+  const bsc_layout layout = (bsc_layout)p->layout;
+  switch (p->kind) {
+    case BSC_QUANT_ROWWISE: {
+      bool empty;
+      bsc_status s = check_shape(p->B, p->S, p->H, p->D, p->layout, &empty);
+      if (s != BSC_OK || empty) return s;
+      if (!p->x || !p->e4m3 || !p->sc) return BSC_ERR_NULL;
+      if (!aligned16(p->x) || !aligned16(p->e4m3) || !aligned16(p->sc)) return BSC_ERR_ALIGN;
+      if ((s = check_device()) != BSC_OK) return s;
+      return from_cuda(bsc::launch_quant_rowwise(p->x, p->e4m3, p->sc, p->B, p->S, p->H, p->layout,
+                                                 reinterpret_cast<cudaStream_t>(stream), p->rule));
+    }
+    case BSC_QUANT_V_COLWISE:
+      return quant_v_common(p->x, p->B, p->S, p->H, p->D, layout, p->e4m3, p->sc, nullptr, nullptr, stream, true,
+                            false, p->rule);
+    case BSC_QUANT_V_TOKEN_NORM:
+      return quant_v_common(p->x, p->B, p->S, p->H, p->D, layout, nullptr, nullptr, p->vtn_e4m3, p->vtn_sc, stream,
+                            false, true, p->rule);
+    case BSC_QUANT_V_FUSED:
+      return quant_v_common(p->x, p->B, p->S, p->H, p->D, layout, p->e4m3, p->sc, p->vtn_e4m3, p->vtn_sc, stream,
+                            true, true, p->rule);
+    default:
+      return BSC_ERR_UNSUPPORTED;
+  }
 }
 
 bsc_status mxfp8_quantize_v_colwise(const void* v, int B, int S, int H, int D, bsc_layout layout, uint8_t* vt,

@@ -6,10 +6,11 @@
 
 namespace bsc {
 
+// rule: 0 = OCP floor scale rule, 1 = ceil (no element saturates)
 cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, int S, int H, int layout,
-                                 cudaStream_t st);
+                                 cudaStream_t st, int rule = 0);
 cudaError_t launch_quant_v(const void* v, uint8_t* vt, uint8_t* vsc, uint8_t* vtn, uint8_t* vtn_sc, int B, int S,
-                           int H, int layout, cudaStream_t st);
+                           int H, int layout, cudaStream_t st, int rule = 0);
 
 // Everything the attention kernel reads, by value (tensor maps must be 64-byte aligned).
 struct AttnArgs {

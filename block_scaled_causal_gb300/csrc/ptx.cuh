@@ -340,13 +340,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // OCP MX shared exponent for an E4M3 block from the block's absolute maximum (finite):
 // scale byte = clamp(floor(log2 amax) - 8 + 127, 0, 254); zero and fp32-subnormal maxima give 0.
 // Returns the byte; `inv_scale` receives 2^-(byte - 127), an exact power of two.
-__device__ __forceinline__ uint32_t e8m0_from_amax(float amax, float& inv_scale) {
-  const uint32_t ebits = (__float_as_uint(amax) >> 23) & 0xFFu;   // biased fp32 exponent
+__device__ __forceinline__ uint32_t e8m0_from_amax(float amax, float& inv_scale, int ceil_rule = 0) {
+  const uint32_t bits = __float_as_uint(amax);
+  const uint32_t ebits = (bits >> 23) & 0xFFu;                       // biased fp32 exponent
   if (ebits == 0xFFu) {                                              // NaN or Inf in the block
     inv_scale = 0.0f;
     return 0xFFu;
   }
-  const uint32_t sb = ebits > 8u ? ebits - 8u : 0u;                  // (ebits-127) - 8 + 127
+  // floor rule: (ebits-127) - 8 + 127; the ceil rule adds 1 when the significand of amax is above
+  // 1.75 (amax > 448 * 2^e), so that amax * 2^-e <= 448
+  const uint32_t inc = (ceil_rule && ebits > 0u && (bits & 0x7FFFFFu) > 0x600000u) ? 1u : 0u;
+  const uint32_t sb = ebits + inc > 8u ? ebits + inc - 8u : 0u;
   // 2^-(sb-127) = 2^(127-sb): fp32 exponent field 254 - sb (sb in [0,246] -> field in [8,254]).
   inv_scale = __uint_as_float((254u - sb) << 23);
   return sb;

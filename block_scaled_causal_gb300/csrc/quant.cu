@@ -56,7 +56,7 @@ __device__ __forceinline__ uint32_t atom_word_offset(uint32_t m) { return (m & 3
 //   sc[((b*H + h) * T + s/128) * 512 + (s%32)*16 + ((s%128)/32)*4 + c],  c = d / 32.
 __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint4* __restrict__ x, uint2* __restrict__ q,
                                                             uint8_t* __restrict__ sc, long long nrows, int B,
-                                                            int S, int H, int layout) {
+                                                            int S, int H, int layout, int rule) {
   const long long chunk = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = chunk >> 4;
   const bool active = row < nrows;
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint4* __restr
   am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
   am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
   float inv;
-  const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv);
+  const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
   if (active) __stcs(&q[chunk], quant8(v, inv, sb == 0xFFu));
   // gather the 4 block scales of this row on its first thread
   const int lane = threadIdx.x & 31;
@@ -110,7 +110,7 @@ constexpr int VQ_PITCH = 256 + 16;   // bytes per staged token row
 __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
                                                       uint8_t* __restrict__ vsc, uint8_t* __restrict__ vtn,
                                                       uint8_t* __restrict__ vtn_sc, int B, int S, int H,
-                                                      int layout) {
+                                                      int layout, int rule) {
   __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
   const int ntiles = (S + VQ_ROWS - 1) / VQ_ROWS;
   const int tile_idx = blockIdx.x % ntiles;
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
       float inv;
-      const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv);
+      const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
       __stcs(reinterpret_cast<uint2*>(vtn + e), quant8(val, inv, sb == 0xFFu));
       if (l16 == 0) vtn_sc[(long long)plane * S + s0 + r] = (uint8_t)sb;
     }
@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
     asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
   }
   float inv0, inv1;
-  const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0);
-  const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1);
+  const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0, rule);
+  const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1, rule);
   // Byte slot s of the 32-token block holds token perm32(s) = 8*((s%8)/2) + 2*(s/8) + s%2: word i
   // (slots 4i..4i+3) holds tokens k0, k0+1, k0+8, k0+9 with k0 = 16*(i%2) + 2*(i/2).
   uint32_t o0[8], o1[8];
@@ -188,21 +188,21 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
 
 // ------------------------------------------------------------------------------------------
 cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, int S, int H, int layout,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, int rule) {
   const long long nrows = (long long)B * S * H;
   const long long chunks = nrows * 16;
   const unsigned grid = (unsigned)((chunks + 255) / 256);
   quant_rowwise_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(q), sc,
-                                              nrows, B, S, H, layout);
+                                              nrows, B, S, H, layout, rule);
   if (S % 128 != 0) pad_row_atoms_kernel<<<(unsigned)((long long)B * H), 128, 0, st>>>(sc, S);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_v(const void* v, uint8_t* vt, uint8_t* vsc, uint8_t* vtn, uint8_t* vtn_sc, int B, int S,
-                           int H, int layout, cudaStream_t st) {
+                           int H, int layout, cudaStream_t st, int rule) {
   const long long ctas = (long long)B * H * ((S + VQ_ROWS - 1) / VQ_ROWS);
   quant_v_kernel<<<(unsigned)ctas, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(v), vt, vsc, vtn, vtn_sc, B, S,
-                                                  H, layout);
+                                                  H, layout, rule);
   return cudaGetLastError();
 }
 

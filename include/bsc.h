@@ -113,6 +113,37 @@ bsc_status mxfp8_quantize_v_fused(const void* v_bf16, int B, int S, int H, int D
                                   uint8_t* v_e4m3_t, uint8_t* v_sc, uint8_t* vtn_e4m3, uint8_t* vtn_sc,
                                   bsc_stream_t stream);
 
+/*
+ * Scale rule of the quantisers.  FLOOR, used by every call above, is the OCP MX rule stated at
+ * the top of this file.  CEIL rounds the scale up instead, e = ceil(log2(amax / 448)): the
+ * smallest scale at which no element of the block saturates, one more than FLOOR exactly when
+ * the significand of amax is above 1.75.  The pages say only that TE's MXFP8 attention reused
+ * TE's existing quantisation kernels (PR #3865, base change list); CEIL is the "amax / scale
+ * <= 448" reading of such a kernel, offered as a variant.
+ */
+typedef enum { BSC_SCALE_FLOOR = 0, BSC_SCALE_CEIL = 1 } bsc_scale_rule;
+typedef enum {
+  BSC_QUANT_ROWWISE = 0,      /* as mxfp8_quantize_qk_rowwise: x -> e4m3, sc */
+  BSC_QUANT_V_COLWISE = 1,    /* as mxfp8_quantize_v_colwise: x -> e4m3 (the v_e4m3_t), sc */
+  BSC_QUANT_V_TOKEN_NORM = 2, /* as v_token_normalize: x -> vtn_e4m3, vtn_sc */
+  BSC_QUANT_V_FUSED = 3       /* as mxfp8_quantize_v_fused: all four outputs */
+} bsc_quant_kind;
+typedef struct {
+  int kind;               /* bsc_quant_kind */
+  const void* x;          /* [in] bf16 in `layout` */
+  int B, S, H, D;
+  int layout;             /* bsc_layout */
+  int rule;               /* bsc_scale_rule */
+  uint8_t* e4m3;          /* [out] rowwise bytes, or V columnwise bytes [B][H][D][S] */
+  uint8_t* sc;            /* [out] row atoms (rowwise) or column atoms (V columnwise) */
+  uint8_t* vtn_e4m3;      /* [out] token-normalised V bytes (token-norm and fused kinds) */
+  uint8_t* vtn_sc;        /* [out] token amplitudes (token-norm and fused kinds) */
+} bsc_quant_params;
+
+/* Any of the four quantisations above with a chosen scale rule; layouts, sizes, ownership and
+ * errors as in the matching call.  An unknown kind or rule is BSC_ERR_UNSUPPORTED. */
+bsc_status mxfp8_quantize(const bsc_quant_params* p, bsc_stream_t stream);
+
 typedef struct {
   const uint8_t* q;       /* [in] Q E4M3 bytes, `layout`, Hq heads */
   const uint8_t* q_sc;    /* [in] Q row atoms */

@@ -107,6 +107,37 @@ def test_attn_null_params(ops):
     assert ops.lib.bsc_read_device_status(None, None) == 1
 
 
+def test_quant_params_struct_layout(ops):
+    # int, pointer, 6 ints, 4 pointers (LP64)
+    P = ops.QuantParams
+    assert P.x.offset == 8 and P.B.offset == 16 and P.rule.offset == 36 and P.e4m3.offset == 40
+    assert P.vtn_sc.offset == 64 and ctypes.sizeof(P) == 72
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(kind=9), 4),                       # unknown kind
+    (dict(rule=2), 4),                       # unknown rule
+    (dict(S=100), 4),                        # S % 32
+    (dict(layout=5), 2),
+    (dict(x=0), 1),
+    (dict(sc=FAKE + 1), 3),
+    (dict(kind=2, vtn_e4m3=0), 1),           # token-norm needs its own outputs
+    (dict(kind=1, e4m3=FAKE + 8), 3),
+    (dict(kind=3, S=0), 0),                  # empty problem
+    (dict(rule=1, B=0, x=0), 0),
+])
+def test_quant_entry_validation(ops, kw, want):
+    base = dict(kind=0, x=FAKE, B=1, S=128, H=2, D=128, layout=0, rule=1, e4m3=FAKE, sc=FAKE,
+                vtn_e4m3=FAKE, vtn_sc=FAKE)
+    base.update(kw)
+    p = ops.QuantParams(**base)
+    assert ops.lib.mxfp8_quantize(ctypes.byref(p), None) == want
+
+
+def test_quant_entry_null(ops):
+    assert ops.lib.mxfp8_quantize(None, None) == 1
+
+
 def test_perm32_is_an_involution_within_blocks():
     import numpy as np
     from tests._helpers import perm32, vt_to_token_order
