@@ -422,20 +422,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       // E4M3 P (scale 2^-P_SHIFT; a second term holds the residual at 2^-4 of that) over this S
       // buffer: block kb's columns 8kb + 2qd and 8kb + 2qd + 1 carry keys {8(4kb) + 2qd + e,
-      // 8(4kb+1) + 2qd + e} and {8(4kb+2) ..., 8(4kb+3) ...}.  In the diagonal tile the own and later
-      // 32-key blocks are 0 (the leaky control keeps the own block on this path instead).
-      const int fp8_limit = diag ? (LEAKY ? q + 1 : q) : 4;
+      // 8(4kb+1) + 2qd + e} and {8(4kb+2) ..., 8(4kb+3) ...}.  In the diagonal tile the blocks after
+      // the own block are masked to 0 already; the own block's words are cleared below (the leaky
+      // control keeps the own block on this path instead).
       uint32_t w0[16], w1[16];
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
-        const bool use = kb < fp8_limit;
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int k0 = 4 * kb + 2 * c2;   // keys 8k0 + 2qd + e and 8(k0+1) + 2qd + e
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
-            const float p0 = use ? v[4 * k0 + 2 * rr] : 0.f, p1 = use ? v[4 * k0 + 2 * rr + 1] : 0.f;
-            const float p2 = use ? v[4 * k0 + 4 + 2 * rr] : 0.f, p3 = use ? v[4 * k0 + 4 + 2 * rr + 1] : 0.f;
+            const float p0 = v[4 * k0 + 2 * rr], p1 = v[4 * k0 + 2 * rr + 1];
+            const float p2 = v[4 * k0 + 4 + 2 * rr], p3 = v[4 * k0 + 4 + 2 * rr + 1];
             const uint16_t h01 = cvt_e4m3x2(p0, p1), h23 = cvt_e4m3x2(p2, p3);
             w0[4 * kb + 2 * rr + c2] = (uint32_t)h01 | ((uint32_t)h23 << 16);
             if (P_TERMS > 1) {
@@ -446,6 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               const float d3 = p3 - __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
               w1[4 * kb + 2 * rr + c2] =
                   (uint32_t)cvt_e4m3x2(d0 * 16.f, d1 * 16.f) | ((uint32_t)cvt_e4m3x2(d2 * 16.f, d3 * 16.f) << 16);
+            }
+          }
+        }
+      }
+      if (diag && !LEAKY) {
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+          if (kb == q) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              w0[4 * kb + i] = 0u;
+              w1[4 * kb + i] = 0u;
             }
           }
         }
