@@ -237,9 +237,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step(p_terms, ev_mid, out8=False):
-        ops.mxfp8_quantize_qk_rowwise(q, w.layout, out=qq, out_sc=qs, stream=stream)
-        ops.mxfp8_quantize_qk_rowwise(k, w.layout, out=kq, out_sc=ks, stream=stream)
-        ops.mxfp8_quantize_v_fused(v, w.layout, out=(vt, vsc, vtn, vtn_sc), stream=stream)
+        ops.mxfp8_quantize_qkv(q, k, v, w.layout, out=(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc), stream=stream)
         ev_mid.record(stream)
         if out8:   # MXFP8 O (E4M3 + one UE8M0 scale per 32 d) instead of BF16 O
             ops.mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, w.layout, w.scale, p_terms=p_terms,
@@ -423,7 +421,7 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk,
         "quant_ms": sum(quant_ms) / len(quant_ms),
         "attn_ms": attn_avg,

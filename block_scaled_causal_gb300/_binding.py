@@ -37,6 +37,8 @@ def _load():
     lib.mxfp8_quantize_v_fused.argtypes = [vp, i32, i32, i32, i32, i32, u8p, u8p, u8p, u8p, vp]
     lib.mxfp8_causal_attn_fwd.restype = i32
     lib.mxfp8_causal_attn_fwd.argtypes = [ctypes.POINTER(AttnFwdParams), vp]
+    lib.mxfp8_quantize_qkv.restype = i32
+    lib.mxfp8_quantize_qkv.argtypes = [ctypes.POINTER(QkvQuantParams), vp]
     lib.mxfp8_quantize.restype = i32
     lib.mxfp8_quantize.argtypes = [ctypes.POINTER(QuantParams), vp]
     lib.bf16_attn_bwd.restype = i32
@@ -70,6 +72,18 @@ class QuantParams(ctypes.Structure):
         ("B", ctypes.c_int), ("S", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int),
         ("layout", ctypes.c_int), ("rule", ctypes.c_int),
         ("e4m3", ctypes.c_void_p), ("sc", ctypes.c_void_p),
+        ("vtn_e4m3", ctypes.c_void_p), ("vtn_sc", ctypes.c_void_p),
+    ]
+
+
+class QkvQuantParams(ctypes.Structure):
+    """Mirror of bsc_qkv_quant_params."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("S", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
+        ("layout", ctypes.c_int), ("rule", ctypes.c_int),
+        ("q_e4m3", ctypes.c_void_p), ("q_sc", ctypes.c_void_p), ("k_e4m3", ctypes.c_void_p), ("k_sc", ctypes.c_void_p),
+        ("v_e4m3_t", ctypes.c_void_p), ("v_sc", ctypes.c_void_p),
         ("vtn_e4m3", ctypes.c_void_p), ("vtn_sc", ctypes.c_void_p),
     ]
 
@@ -233,13 +247,7 @@ def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, o=None
     then the leak-free causal attention forward.  Returns (O bf16, LSE fp32); `o` and `lse` may be
     given (laid out like q and [B, Hq, S]).  With o8_out=True the MXFP8 O is returned as well, as
     in mxfp8_causal_attn_fwd."""
-    qq, qs = mxfp8_quantize_qk_rowwise(q, layout, stream=stream)
-    kq, ks = mxfp8_quantize_qk_rowwise(k, layout, stream=stream)
-    if leaky:
-        vt, vsc = mxfp8_quantize_v_colwise(v, layout, stream=stream)
-        vtn = vtn_sc = None
-    else:
-        vt, vsc, vtn, vtn_sc = mxfp8_quantize_v_fused(v, layout, stream=stream)
+    qq, qs, kq, ks, vt, vsc, vtn, vtn_sc = mxfp8_quantize_qkv(q, k, v, layout, token_norm=not leaky, stream=stream)
     return mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, p_terms, leaky,
                                  o=o, lse=lse, stream=stream, o8_out=o8_out, bf16_out=bf16_out)
 
@@ -269,9 +277,7 @@ def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softma
 def forward_backward(q, k, v, do, layout=BSHD, softmax_scale=None, stream=None):
     """Forward (one E4M3 term for P) then the backward on decoded operands; returns
     (O, LSE, dQ, dK, dV)."""
-    qq, qs = mxfp8_quantize_qk_rowwise(q, layout, stream=stream)
-    kq, ks = mxfp8_quantize_qk_rowwise(k, layout, stream=stream)
-    vt, vsc, vtn, vtn_sc = mxfp8_quantize_v_fused(v, layout, stream=stream)
+    qq, qs, kq, ks, vt, vsc, vtn, vtn_sc = mxfp8_quantize_qkv(q, k, v, layout, stream=stream)
     o, lse = mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, stream=stream)
     dq, dk, dv = bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o, lse, do, layout, softmax_scale, stream=stream)
     return o, lse, dq, dk, dv
@@ -300,3 +306,29 @@ def mxfp8_quantize(kind, x, layout=BSHD, rule=SCALE_FLOOR, stream=None):
     if kind == QUANT_V_TOKEN_NORM:
         return vtn, vtn_sc
     return e4m3, sc
+
+
+def mxfp8_quantize_qkv(q, k, v, layout=BSHD, rule=SCALE_FLOOR, token_norm=True, out=None, stream=None):
+    """Q and K rowwise and V columnwise (+ token-normalised unless token_norm=False) in one launch.
+    Returns (q_e4m3, q_sc, k_e4m3, k_sc, v_e4m3_t, v_sc, vtn_e4m3, vtn_sc), the last two None when
+    token_norm=False; `out` may give all eight (the last two may be None)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, torch.bfloat16, n)
+    B, S, Hq, D = _bshd_dims(q, layout)
+    Hkv = _bshd_dims(k, layout)[2]
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("k and v must have the same shape")
+    T = (S + 127) // 128
+    if out is None:
+        u8 = dict(dtype=torch.uint8, device=q.device)
+        out = (torch.empty(q.shape, **u8), torch.empty((B, Hq, T, 512), **u8),
+               torch.empty(k.shape, **u8), torch.empty((B, Hkv, T, 512), **u8),
+               torch.empty((B, Hkv, D, S), **u8), torch.empty((B, Hkv, T, 512), **u8),
+               torch.empty(v.shape, **u8) if token_norm else None,
+               torch.empty((B, Hkv, S), **u8) if token_norm else None)
+    qq, qs, kq, ks, vt, vsc, vtn, vtn_sc = out
+    p = QkvQuantParams(q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), B=B, S=S, Hq=Hq, Hkv=Hkv, D=D, layout=layout,
+                       rule=rule, q_e4m3=_ptr(qq), q_sc=_ptr(qs), k_e4m3=_ptr(kq), k_sc=_ptr(ks), v_e4m3_t=_ptr(vt),
+                       v_sc=_ptr(vsc), vtn_e4m3=_ptr(vtn), vtn_sc=_ptr(vtn_sc))
+    _check(lib.mxfp8_quantize_qkv(ctypes.byref(p), _stream(stream)))
+    return qq, qs, kq, ks, vt, vsc, vtn, vtn_sc

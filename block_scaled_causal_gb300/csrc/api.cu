@@ -200,6 +200,47 @@ bsc_status mxfp8_quantize_v_fused(const void* v, int B, int S, int H, int D, bsc
   return quant_v_common(v, B, S, H, D, layout, vt, vsc, vtn, vtn_sc, stream, true, true);
 }
 
+bsc_status mxfp8_quantize_qkv(const bsc_qkv_quant_params* p, bsc_stream_t stream) {
+  if (!p) return BSC_ERR_NULL;
+  if (p->Hq < 0 || p->Hkv < 0) return BSC_ERR_SHAPE;
+  if (p->rule != BSC_SCALE_FLOOR && p->rule != BSC_SCALE_CEIL) return BSC_ERR_UNSUPPORTED;
+  bool empty;
+  bsc_status s = check_shape(p->B, p->S, p->Hq, p->D, p->layout, &empty);
+  if (s != BSC_OK) return s;
+  if (!empty && p->Hkv == 0) return BSC_ERR_SHAPE;
+  if (empty) return BSC_OK;
+  if (p->Hq % p->Hkv != 0) return BSC_ERR_SHAPE;
+  const bool col = p->v_e4m3_t != nullptr || p->v_sc != nullptr;
+  const bool tn = p->vtn_e4m3 != nullptr || p->vtn_sc != nullptr;
+  if (!p->q || !p->k || !p->v || !p->q_e4m3 || !p->q_sc || !p->k_e4m3 || !p->k_sc) return BSC_ERR_NULL;
+  if ((col && (!p->v_e4m3_t || !p->v_sc)) || (tn && (!p->vtn_e4m3 || !p->vtn_sc)) || (!col && !tn))
+    return BSC_ERR_NULL;
+  for (const void* ptr : {p->q, p->k, p->v, (const void*)p->q_e4m3, (const void*)p->q_sc, (const void*)p->k_e4m3,
+                          (const void*)p->k_sc, (const void*)p->v_e4m3_t, (const void*)p->v_sc,
+                          (const void*)p->vtn_e4m3, (const void*)p->vtn_sc})
+    if (!aligned16(ptr)) return BSC_ERR_ALIGN;
+  if ((s = check_device()) != BSC_OK) return s;
+  bsc::QkvQuantArgs a{};
+  a.q = p->q;
+  a.k = p->k;
+  a.v = p->v;
+  a.B = p->B;
+  a.S = p->S;
+  a.Hq = p->Hq;
+  a.Hkv = p->Hkv;
+  a.layout = p->layout;
+  a.rule = p->rule;
+  a.q8 = p->q_e4m3;
+  a.q_sc = p->q_sc;
+  a.k8 = p->k_e4m3;
+  a.k_sc = p->k_sc;
+  a.vt = p->v_e4m3_t;
+  a.vsc = p->v_sc;
+  a.vtn = p->vtn_e4m3;
+  a.vtn_sc = p->vtn_sc;
+  return from_cuda(bsc::launch_quant_qkv(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stream) {
   if (!p) return BSC_ERR_NULL;
   if (p->Hq < 0 || p->Hkv < 0) return BSC_ERR_SHAPE;

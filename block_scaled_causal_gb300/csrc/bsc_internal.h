@@ -9,6 +9,23 @@ namespace bsc {
 // rule: 0 = OCP floor scale rule, 1 = ceil (no element saturates)
 cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, int S, int H, int layout,
                                  cudaStream_t st, int rule = 0);
+// Q and K rowwise and V (columnwise and/or token-normalised) in one launch.
+struct QkvQuantArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, S, Hq, Hkv, layout, rule;
+  uint8_t* q8;
+  uint8_t* q_sc;
+  uint8_t* k8;
+  uint8_t* k_sc;
+  uint8_t* vt;       // may be nullptr (no columnwise copy)
+  uint8_t* vsc;
+  uint8_t* vtn;      // may be nullptr (no token-normalised copy)
+  uint8_t* vtn_sc;
+  long long nv_blocks, nq_blocks;   // set by the launcher
+};
+cudaError_t launch_quant_qkv(QkvQuantArgs a, cudaStream_t st);
 cudaError_t launch_quant_v(const void* v, uint8_t* vt, uint8_t* vsc, uint8_t* vtn, uint8_t* vtn_sc, int B, int S,
                            int H, int layout, cudaStream_t st, int rule = 0);
 

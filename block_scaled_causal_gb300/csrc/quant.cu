@@ -50,39 +50,59 @@ __device__ __forceinline__ uint2 quant8(const uint4& v, float inv, bool nonfinit
 __device__ __forceinline__ uint32_t atom_word_offset(uint32_t m) { return (m & 31u) * 16u + ((m >> 5) & 3u) * 4u; }
 
 // ------------------------------------------------------------------------------------------
-// Rowwise quantiser (Q, K): one thread per 16 bytes (8 elements); 16 threads per 128-element row;
-// a 32-element block is 4 adjacent threads.  Rows are visited in memory order; (b, s, h) of a row
-// follows from the layout.  Scale words go to the atom layout, T = ceil(S/128) atoms per (b, h):
+// Rowwise quantiser (Q, K): a CTA of 256 threads takes 64 consecutive tokens s0..s0+63 of one
+// (b, h) plane; a token row is 256 bytes = 16 threads x 16 bytes (8 elements) and a 32-element
+// block is 4 adjacent threads.  Each thread loads its four chunks (rows s0 + 16i + tid/16) before
+// converting any, so that 64 bytes per thread are in flight.  Scale words go to the atom layout,
+// T = ceil(S/128) atoms per (b, h):
 //   sc[((b*H + h) * T + s/128) * 512 + (s%32)*16 + ((s%128)/32)*4 + c],  c = d / 32.
-__global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint4* __restrict__ x, uint2* __restrict__ q,
-                                                            uint8_t* __restrict__ sc, long long nrows, int B,
-                                                            int S, int H, int layout, int rule) {
-  const long long chunk = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = chunk >> 4;
-  const bool active = row < nrows;
-  const uint4 v = active ? __ldcs(&x[chunk]) : make_uint4(0, 0, 0, 0);
-  uint32_t am = absmax_bits8(v);
-  am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-  am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-  float inv;
-  const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
-  if (active) __stcs(&q[chunk], quant8(v, inv, sb == 0xFFu));
-  // gather the 4 block scales of this row on its first thread
-  const int lane = threadIdx.x & 31;
-  const int base = lane & 16;
-  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, base + 4);
-  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 8);
-  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 12);
-  if (active && (lane & 15) == 0) {
-    long long b, s, h;
-    h = row % H;
-    const long long r2 = row / H;
-    if (layout == 0) { s = r2 % S; b = r2 / S; }
-    else { b = r2 % B; s = r2 / B; }
-    const long long plane = b * H + h;
-    const long long off = (plane * ((S + 127) / 128) + s / 128) * 512 + atom_word_offset((uint32_t)(s & 127));
-    *reinterpret_cast<uint32_t*>(sc + off) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+constexpr int RW_ROWS = 64;
+
+// `blk` = plane * ceil(S/64) + s-chunk.
+__device__ __forceinline__ void rowwise_rows(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
+                                             uint8_t* __restrict__ sc, int B, int S, int H, int layout, int rule,
+                                             long long blk) {
+  const int nchunk = (S + RW_ROWS - 1) / RW_ROWS;
+  const long long plane = blk / nchunk;
+  const int s0 = (int)(blk - plane * nchunk) * RW_ROWS;
+  const long long h = plane % H, b = plane / H;
+  const long long row_stride = layout == 0 ? (long long)H * 128 : (long long)B * H * 128;   // elements per s
+  const long long base0 = layout == 0 ? ((b * S) * H + h) * 128 : (b * H + h) * 128;
+  const int tid = threadIdx.x, l16 = tid & 15, lane = tid & 31;
+  uint4 v[4];
+  long long e[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = s0 + 16 * i + (tid >> 4);
+    e[i] = base0 + (long long)s * row_stride + l16 * 8;
+    v[i] = s < S ? __ldcs(reinterpret_cast<const uint4*>(x + e[i] * 2)) : make_uint4(0, 0, 0, 0);
   }
+  const int T = (S + 127) / 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = s0 + 16 * i + (tid >> 4);
+    uint32_t am = absmax_bits8(v[i]);
+    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+    float inv;
+    const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
+    if (s < S) __stcs(reinterpret_cast<uint2*>(q + e[i]), quant8(v[i], inv, sb == 0xFFu));
+    // gather the 4 block scales of this row on its first thread
+    const int base = lane & 16;
+    const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, base + 4);
+    const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 8);
+    const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 12);
+    if (s < S && l16 == 0) {
+      const long long off = (plane * T + s / 128) * 512 + atom_word_offset((uint32_t)(s & 127));
+      *reinterpret_cast<uint32_t*>(sc + off) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
+                                                            uint8_t* __restrict__ sc, int B, int S, int H,
+                                                            int layout, int rule) {
+  rowwise_rows(x, q, sc, B, S, H, layout, rule, blockIdx.x);
 }
 
 // Rows S..T*128-1 of the last row atom of each (b, h) hold no token: their scale words are 0.
@@ -107,14 +127,15 @@ __global__ void __launch_bounds__(128) pad_row_atoms_kernel(uint8_t* __restrict_
 constexpr int VQ_ROWS = 128;
 constexpr int VQ_PITCH = 256 + 16;   // bytes per staged token row
 
-__global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
-                                                      uint8_t* __restrict__ vsc, uint8_t* __restrict__ vtn,
-                                                      uint8_t* __restrict__ vtn_sc, int B, int S, int H,
-                                                      int layout, int rule) {
-  __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
+// `blk` is the (b, h, tile) index; `tile` is VQ_ROWS x VQ_PITCH bytes of shared memory.  The
+// whole CTA takes part.
+__device__ __forceinline__ void v_tile(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+                                       uint8_t* __restrict__ vsc, uint8_t* __restrict__ vtn,
+                                       uint8_t* __restrict__ vtn_sc, int B, int S, int H, int layout, int rule,
+                                       int blk, uint8_t* tile) {
   const int ntiles = (S + VQ_ROWS - 1) / VQ_ROWS;
-  const int tile_idx = blockIdx.x % ntiles;
-  const int plane = blockIdx.x / ntiles;   // b*H + h
+  const int tile_idx = blk % ntiles;
+  const int plane = blk / ntiles;   // b*H + h
   const int h = plane % H, b = plane / H;
   const int s0 = tile_idx * VQ_ROWS;
   const int tid = threadIdx.x;
@@ -186,15 +207,52 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
   atom[atom_word_offset(d1) + kb] = valid ? (uint8_t)sb1 : (uint8_t)0;
 }
 
+__global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+                                                      uint8_t* __restrict__ vsc, uint8_t* __restrict__ vtn,
+                                                      uint8_t* __restrict__ vtn_sc, int B, int S, int H,
+                                                      int layout, int rule) {
+  __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
+  v_tile(v, vt, vsc, vtn, vtn_sc, B, S, H, layout, rule, (int)blockIdx.x, tile);
+}
+
+// ------------------------------------------------------------------------------------------
+// Q, K and V in one launch: CTAs [0, nv) take V tiles, then Q's 64-token chunks, then K's.  Each
+// CTA does exactly what the matching kernel above does for the same index.
+__global__ void __launch_bounds__(256) quant_qkv_kernel(const __grid_constant__ QkvQuantArgs a) {
+  __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
+  const long long blk = blockIdx.x;
+  if (blk < a.nv_blocks) {
+    v_tile(reinterpret_cast<const uint8_t*>(a.v), a.vt, a.vsc, a.vtn, a.vtn_sc, a.B, a.S, a.Hkv, a.layout, a.rule,
+           (int)blk, tile);
+  } else if (blk < a.nv_blocks + a.nq_blocks) {
+    rowwise_rows(reinterpret_cast<const uint8_t*>(a.q), a.q8, a.q_sc, a.B, a.S, a.Hq, a.layout, a.rule,
+                 blk - a.nv_blocks);
+  } else {
+    rowwise_rows(reinterpret_cast<const uint8_t*>(a.k), a.k8, a.k_sc, a.B, a.S, a.Hkv, a.layout, a.rule,
+                 blk - a.nv_blocks - a.nq_blocks);
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, int S, int H, int layout,
                                  cudaStream_t st, int rule) {
-  const long long nrows = (long long)B * S * H;
-  const long long chunks = nrows * 16;
-  const unsigned grid = (unsigned)((chunks + 255) / 256);
-  quant_rowwise_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(q), sc,
-                                              nrows, B, S, H, layout, rule);
+  const long long grid = (long long)B * H * ((S + RW_ROWS - 1) / RW_ROWS);
+  quant_rowwise_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(x), q, sc, B, S, H, layout,
+                                                        rule);
   if (S % 128 != 0) pad_row_atoms_kernel<<<(unsigned)((long long)B * H), 128, 0, st>>>(sc, S);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_qkv(QkvQuantArgs a, cudaStream_t st) {
+  const long long nchunk = (a.S + RW_ROWS - 1) / RW_ROWS;
+  a.nv_blocks = (long long)a.B * a.Hkv * ((a.S + VQ_ROWS - 1) / VQ_ROWS);
+  a.nq_blocks = (long long)a.B * a.Hq * nchunk;
+  const long long nk_blocks = (long long)a.B * a.Hkv * nchunk;
+  quant_qkv_kernel<<<(unsigned)(a.nv_blocks + a.nq_blocks + nk_blocks), 256, 0, st>>>(a);
+  if (a.S % 128 != 0) {
+    pad_row_atoms_kernel<<<(unsigned)((long long)a.B * a.Hq), 128, 0, st>>>(a.q_sc, a.S);
+    pad_row_atoms_kernel<<<(unsigned)((long long)a.B * a.Hkv), 128, 0, st>>>(a.k_sc, a.S);
+  }
   return cudaGetLastError();
 }
 

@@ -144,6 +144,37 @@ typedef struct {
  * errors as in the matching call.  An unknown kind or rule is BSC_ERR_UNSUPPORTED. */
 bsc_status mxfp8_quantize(const bsc_quant_params* p, bsc_stream_t stream);
 
+/*
+ * Every operand of the attention forward quantised in one launch: Q and K rowwise (as
+ * mxfp8_quantize_qk_rowwise), V columnwise and token-normalised (as mxfp8_quantize_v_fused), each
+ * tensor read once.  Outputs are byte-identical to those calls.  The pages quantise the three
+ * operands in a separate step ahead of the attention and count it, with the launches, in a fixed
+ * cost of about 1 ms at batch 1 (PR #3865, Performance); one launch for all three is this
+ * library's form of that step.
+ *   q [in] bf16 B x S x Hq x D in `layout`;  k, v [in] bf16 with Hkv heads;  Hq % Hkv == 0.
+ *   q_e4m3, q_sc, k_e4m3, k_sc [out] as mxfp8_quantize_qk_rowwise for Q and K.
+ *   v_e4m3_t, v_sc [out] as mxfp8_quantize_v_colwise; vtn_e4m3, vtn_sc [out] as v_token_normalize.
+ *   Either V pair may be NULL (both pointers of the pair), not both.
+ *   rule: bsc_scale_rule.  Errors as the calls above; an unknown rule is BSC_ERR_UNSUPPORTED.
+ */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, S, Hq, Hkv, D;
+  int layout;             /* bsc_layout */
+  int rule;               /* bsc_scale_rule */
+  uint8_t* q_e4m3;
+  uint8_t* q_sc;
+  uint8_t* k_e4m3;
+  uint8_t* k_sc;
+  uint8_t* v_e4m3_t;
+  uint8_t* v_sc;
+  uint8_t* vtn_e4m3;
+  uint8_t* vtn_sc;
+} bsc_qkv_quant_params;
+bsc_status mxfp8_quantize_qkv(const bsc_qkv_quant_params* p, bsc_stream_t stream);
+
 typedef struct {
   const uint8_t* q;       /* [in] Q E4M3 bytes, `layout`, Hq heads */
   const uint8_t* q_sc;    /* [in] Q row atoms */

@@ -136,6 +136,34 @@ def test_quant_entry_validation(ops, kw, want):
 
 def test_quant_entry_null(ops):
     assert ops.lib.mxfp8_quantize(None, None) == 1
+    assert ops.lib.mxfp8_quantize_qkv(None, None) == 1
+
+
+def test_qkv_quant_params_struct_layout(ops):
+    P = ops.QkvQuantParams
+    assert P.B.offset == 24 and P.rule.offset == 48 and P.q_e4m3.offset == 56 and P.vtn_sc.offset == 112
+    assert ctypes.sizeof(P) == 120
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(rule=3), 4),
+    (dict(Hq=3), 2),                                 # Hq % Hkv
+    (dict(Hkv=0), 2),
+    (dict(S=96 + 8), 4),
+    (dict(layout=4), 2),
+    (dict(q=0), 1),
+    (dict(vtn_e4m3=0), 1),                           # half a V pair
+    (dict(v_e4m3_t=0, v_sc=0, vtn_e4m3=0, vtn_sc=0), 1),   # no V output at all
+    (dict(k_sc=FAKE + 4), 3),
+    (dict(S=0), 0),
+    (dict(B=0, q=0, k=0, v=0), 0),
+])
+def test_qkv_quant_validation(ops, kw, want):
+    base = dict(q=FAKE, k=FAKE, v=FAKE, B=1, S=128, Hq=4, Hkv=2, D=128, layout=0, rule=0, q_e4m3=FAKE, q_sc=FAKE,
+                k_e4m3=FAKE, k_sc=FAKE, v_e4m3_t=FAKE, v_sc=FAKE, vtn_e4m3=FAKE, vtn_sc=FAKE)
+    base.update(kw)
+    p = ops.QkvQuantParams(**base)
+    assert ops.lib.mxfp8_quantize_qkv(ctypes.byref(p), None) == want
 
 
 def test_perm32_is_an_involution_within_blocks():
