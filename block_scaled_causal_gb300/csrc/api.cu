@@ -316,7 +316,8 @@ bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
   if (!encode_tokens_map(&a.tm_q, p->q, p->B, p->S, p->Hq, p->layout, true) ||
       !encode_tokens_map(&a.tm_k, p->k, p->B, p->S, p->Hkv, p->layout, true) ||
       !encode_tokens_map(&a.tm_vtn, p->vtn, p->B, p->S, p->Hkv, p->layout, false) ||
-      !encode_bf16_tokens_map(&a.tm_do, p->d_o, p->B, p->S, p->Hq, p->layout))
+      !encode_bf16_tokens_map(&a.tm_do, p->d_o, p->B, p->S, p->Hq, p->layout) ||
+      !encode_bf16_tokens_map(&a.tm_o, p->o, p->B, p->S, p->Hq, p->layout))
     return BSC_ERR_CUDA;
   a.q_sc = p->q_sc;
   a.k_sc = p->k_sc;

@@ -102,6 +102,35 @@ __device__ __forceinline__ void row_stats(const BwdArgs& a, int b, int hq, int i
   }
 }
 
+// The same statistics from shared memory: the BF16 tiles of dO and O (TMA zero-fills rows past
+// S) and the tile's LSE values (copied for the rows below S only).
+__device__ __forceinline__ void row_stats_tiles(const BwdArgs& a, int it, const uint8_t* do_tile,
+                                                const uint8_t* o_tile, const float* lse_tile, float* lse2,
+                                                float* dlt) {
+  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int i = it * BM + r;
+  float acc = 0.f;
+  if (i < a.S) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t off = bf_off((uint32_t)r, (uint32_t)(64 * half + 8 * c));
+      const uint4 x = *reinterpret_cast<const uint4*>(o_tile + off);
+      const uint4 y = *reinterpret_cast<const uint4*>(do_tile + off);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+  if (half == 0) {
+    dlt[r] = i < a.S ? acc : 0.f;
+    lse2[r] = i < a.S ? lse_tile[r] * 1.4426950408889634f : INFINITY;
+  }
+}
+
 // E4M3 tile [row][d] (TMA, 128-byte swizzle) with row-atom scales -> BF16 [row][d].  Rows at or
 // past `nrows` become 0.
 __device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* sc_atom, uint8_t* dst, int nrows) {
@@ -248,12 +277,13 @@ constexpr uint32_t KV_Q = KV_Q8 + 16384;      // Q bf16 [q][d]
 constexpr uint32_t KV_DO = KV_Q + 32768;      // dO bf16 [q][d]
 constexpr uint32_t KV_P = KV_DO + 32768;      // P bf16 [q][key] (the V bytes [key][d] before that)
 constexpr uint32_t KV_VN8 = KV_P;
-constexpr uint32_t KV_DS = KV_P + 32768;      // dS bf16 [q][key]
+constexpr uint32_t KV_DS = KV_P + 32768;      // dS bf16 [q][key] (O bf16 [q][d] before that)
 constexpr uint32_t KV_SFQ = KV_DS + 32768;
 constexpr uint32_t KV_SFK = KV_SFQ + 512;
 constexpr uint32_t KV_AMP = KV_SFK + 512;
 constexpr uint32_t KV_STAT = KV_AMP + 128;    // [2 buffers][LSE | Dlt][128] floats
-constexpr uint32_t KV_BAR = KV_STAT + 2048;
+constexpr uint32_t KV_LSE = KV_STAT + 2048;
+constexpr uint32_t KV_BAR = KV_LSE + 512;
 constexpr uint32_t KV_MISC = KV_BAR + 64;
 constexpr uint32_t KV_SMEM = KV_MISC + 16 + 1024;
 static_assert(KV_SMEM <= 227 * 1024, "shared memory budget");
@@ -293,17 +323,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, a.dev_status, a.limit_ns};
   const bool leader = threadIdx.x == 0;
-  auto hq_of = [&](int n) { return hk * g + n / (T - jt); };
-  auto it_of = [&](int n) { return jt + n % (T - jt); };
+  // Query tiles from the last down to the key tile, the group's heads innermost: CTAs of one KV head
+  // that run at the same time then read the same Q, dO and O tiles, which stay in L2.
+  auto hq_of = [&](int n) { return hk * g + n % g; };
+  auto it_of = [&](int n) { return T - 1 - n / g; };
   auto load_q = [&](int n) {
     mbar_arrive_expect_tx(bar(KB_Q), BM * HD + 512);
     tma_load_4d(sbase + KV_Q8, &a.tm_q, bar(KB_Q), 0, hq_of(n), it_of(n) * BM, b);
     bulk_load(sbase + KV_SFQ, a.q_sc + (((long long)b * a.Hq + hq_of(n)) * T + it_of(n)) * 512, 512, bar(KB_Q));
   };
+  // dO into its tile and O into the dS tile (read for the row statistics before dS is written)
   auto load_do = [&](int n) {
-    mbar_arrive_expect_tx(bar(KB_DO), 2 * BM * HD);
-    tma_load_4d(sbase + KV_DO, &a.tm_do, bar(KB_DO), 0, hq_of(n), it_of(n) * BM, b);
-    tma_load_4d(sbase + KV_DO + ATOM, &a.tm_do, bar(KB_DO), 64, hq_of(n), it_of(n) * BM, b);
+    const int it = it_of(n);
+    const uint32_t lse_bytes = 4u * (uint32_t)min(BM, a.S - it * BM);
+    mbar_arrive_expect_tx(bar(KB_DO), 4 * BM * HD + lse_bytes);
+    tma_load_4d(sbase + KV_DO, &a.tm_do, bar(KB_DO), 0, hq_of(n), it * BM, b);
+    tma_load_4d(sbase + KV_DO + ATOM, &a.tm_do, bar(KB_DO), 64, hq_of(n), it * BM, b);
+    tma_load_4d(sbase + KV_DS, &a.tm_o, bar(KB_DO), 0, hq_of(n), it * BM, b);
+    tma_load_4d(sbase + KV_DS + ATOM, &a.tm_o, bar(KB_DO), 64, hq_of(n), it * BM, b);
+    bulk_load(sbase + KV_LSE, a.lse + ((long long)b * a.Hq + hq_of(n)) * a.S + (long long)it * BM, lse_bytes,
+              bar(KB_DO));
   };
   bool ok = true;
   int q_issued = 0, q_seen = 0, do_issued = 0, do_seen = 0;
@@ -319,7 +358,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     load_do(0);
   }
   q_issued = do_issued = 1;
-  row_stats(a, b, hq_of(0), it_of(0), stat(0), stat(0) + 128);
   ok = cta_all(mbar_wait(bar(KB_KV), 0, ctl, W_KV));
   const bool kv_seen = ok;
   if (ok) decode_vt(smem + KV_VN8, smem + KV_AMP, smem + KV_V, nkeys);
@@ -358,14 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       mma_bf16_k128<false, false>(tmem + T_DP, sbase + KV_DO, sbase + KV_V, false);   // dP = dO V^T
       tc_commit(bar(KB_MMA3));
     }
+    // LSE and Dlt of this query tile while dP computes (dO and O are in shared memory by now)
+    if (ok) row_stats_tiles(a, it, smem + KV_DO, smem + KV_DS, reinterpret_cast<const float*>(smem + KV_LSE), lse2, dlt);
+    __syncthreads();   // O's tile is read before dS overwrites it
     float p[64];
     if (ok) {
       compute_p(tmem, rv, lse2, a.scale_log2e, it == jt, p);
       store_rows(smem + KV_P, rv, p);
-    }
-    if (n + 1 < n_iter) {
-      float* nx = stat((n + 1) & 1);
-      row_stats(a, b, hq_of(n + 1), it_of(n + 1), nx, nx + 128);
     }
     if (ok) ok = mbar_wait(bar(KB_MMA3), par, ctl, W_MMA3);
     ok = cta_all(ok);

@@ -60,6 +60,7 @@ struct BwdArgs {
   CUtensorMap tm_k;     // K bytes, as in AttnArgs
   CUtensorMap tm_vtn;   // token-normalised V bytes, as in AttnArgs
   CUtensorMap tm_do;    // dO bf16, 4-D {D, Hq, S, B}, box {64,1,128,1}, 128-byte swizzle
+  CUtensorMap tm_o;     // O bf16, same form as dO
   const uint8_t* q_sc;
   const uint8_t* k_sc;
   const uint8_t* vtn_sc;
