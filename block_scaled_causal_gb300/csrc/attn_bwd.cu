@@ -134,21 +134,37 @@ __device__ __forceinline__ void row_stats_tiles(const BwdArgs& a, int it, const 
 // E4M3 tile [row][d] (TMA, 128-byte swizzle) with row-atom scales -> BF16 [row][d].  Rows at or
 // past `nrows` become 0.
 __device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* sc_atom, uint8_t* dst, int nrows) {
-  for (int unit = threadIdx.x; unit < BM * (HD / 8); unit += kThreads) {
-    const int r = unit >> 4, d0 = (unit & 15) * 8;
-    const uint2 bytes = *reinterpret_cast<const uint2*>(src8 + sw(r, d0));
-    const float s = r < nrows ? pow2_e8m0(sc_atom[atom_byte(r, d0 >> 5)]) : 0.f;
-    *reinterpret_cast<uint4*>(dst + bf_off(r, d0)) = decode8(bytes, s);
+  constexpr int kUnits = BM * (HD / 8) / kThreads;   // 8-element units per thread
+  uint2 bytes[kUnits];
+  float sc[kUnits];
+#pragma unroll
+  for (int u = 0; u < kUnits; ++u) {   // every load first
+    const int unit = threadIdx.x + u * kThreads, r = unit >> 4, d0 = (unit & 15) * 8;
+    bytes[u] = *reinterpret_cast<const uint2*>(src8 + sw(r, d0));
+    sc[u] = r < nrows ? pow2_e8m0(sc_atom[atom_byte(r, d0 >> 5)]) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kUnits; ++u) {
+    const int unit = threadIdx.x + u * kThreads, r = unit >> 4, d0 = (unit & 15) * 8;
+    *reinterpret_cast<uint4*>(dst + bf_off(r, d0)) = decode8(bytes[u], sc[u]);
   }
 }
 // Token-normalised V bytes [key][d] (TMA, no swizzle) with one amplitude per key -> BF16 [key][d].
 // Keys at or past `nkeys` become 0.
 __device__ __forceinline__ void decode_vt(const uint8_t* raw, const uint8_t* amp, uint8_t* dst, int nkeys) {
-  for (int unit = threadIdx.x; unit < BN * (HD / 8); unit += kThreads) {
-    const int key = unit >> 4, d0 = (unit & 15) * 8;
-    const uint2 bytes = *reinterpret_cast<const uint2*>(raw + key * HD + d0);
-    const float s = key < nkeys ? pow2_e8m0(amp[key]) : 0.f;
-    *reinterpret_cast<uint4*>(dst + bf_off(key, d0)) = decode8(bytes, s);
+  constexpr int kUnits = BN * (HD / 8) / kThreads;
+  uint2 bytes[kUnits];
+  float sc[kUnits];
+#pragma unroll
+  for (int u = 0; u < kUnits; ++u) {   // every load first
+    const int unit = threadIdx.x + u * kThreads, key = unit >> 4, d0 = (unit & 15) * 8;
+    bytes[u] = *reinterpret_cast<const uint2*>(raw + key * HD + d0);
+    sc[u] = key < nkeys ? pow2_e8m0(amp[key]) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kUnits; ++u) {
+    const int unit = threadIdx.x + u * kThreads, key = unit >> 4, d0 = (unit & 15) * 8;
+    *reinterpret_cast<uint4*>(dst + bf_off(key, d0)) = decode8(bytes[u], sc[u]);
   }
 }
 
