@@ -1,9 +1,9 @@
 #!/usr/bin/env python
 """Benchmark of the leak-free causal MXFP8 attention forward hot path.
 
-One step = the whole path on one batch of synthetic bf16 inputs already resident in HBM:
-rowwise MXFP8 quantisation of Q and K, the fused V quantisation (columnwise + token-normalised),
-and the attention forward (O bf16 + LSE).  Default workload: B=1, Hq=16, Hkv=4, S=32768, D=128,
+One step = the whole path on one batch of synthetic bf16 inputs already resident in HBM: the
+one-launch MXFP8 quantisation of Q and K (rowwise) and V (columnwise + token-normalised), and the
+attention forward (O bf16 + LSE).  Default workload: B=1, Hq=16, Hkv=4, S=32768, D=128,
 BSHD (the S=32K forward the pages quote).  Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -32,6 +32,22 @@ METRIC = "causal MXFP8 attn fwd TFLOP/s and % of MXFP8 tensor peak at S=32K, 1×
 # quantisation and launch) -> 2*1*16*32768^2*128 / 2.797 ms.
 PAGES_OWN_BLOCK_TFLOPS = 2.0 * 16 * 32768 ** 2 * 128 / 2.797e-3 / 1e12
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
+
+
+def max_over_ranks(x, world, device):
+    """The maximum of a per-rank float over all ranks (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank, world, ms):
+    """Throughput of the whole job: every rank's FLOPs over the (max-over-ranks) step time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 def parse():
@@ -281,18 +297,14 @@ def main():
     step_ms = [a.elapsed_time(c) for a, _, c in evs]
     attn_ms = [b.elapsed_time(c) for _, b, c in evs]
     quant_ms = [a.elapsed_time(b) for a, b, _ in evs]
-    ms_per_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    value = whole_job_tflops(flops, world, ms_per_step)
     attn_avg = sum(attn_ms) / len(attn_ms)
 
     # the same step with two E4M3 terms for P
     evs2 = timed(2, max(3, args.steps // 2), 2)
     torch.cuda.synchronize()
-    ms2 = sum(a.elapsed_time(c) for a, _, c in evs2) / len(evs2)
+    ms2 = max_over_ranks(sum(a.elapsed_time(c) for a, _, c in evs2) / len(evs2), world, dev)
     attn2 = sum(b.elapsed_time(c) for _, b, c in evs2) / len(evs2)
     # backward on decoded operands (BF16 MMAs), inputs resident: the forward's O and LSE and a dO
     g_do = torch.Generator(device="cpu").manual_seed(3)
@@ -312,11 +324,11 @@ def main():
         e1.record(stream)
         bwd_ms.append((e0, e1))
     torch.cuda.synchronize()
-    bwd_avg = sum(a.elapsed_time(b) for a, b in bwd_ms) / len(bwd_ms)
+    bwd_avg = max_over_ranks(sum(a.elapsed_time(b) for a, b in bwd_ms) / len(bwd_ms), world, dev)
     # the same step writing MXFP8 O instead of BF16 O
     evs8 = timed(args.p_terms, max(3, args.steps // 2), 2, out8=True)
     torch.cuda.synchronize()
-    ms8 = sum(a.elapsed_time(c) for a, _, c in evs8) / len(evs8)
+    ms8 = max_over_ranks(sum(a.elapsed_time(c) for a, _, c in evs8) / len(evs8), world, dev)
     attn8 = sum(b.elapsed_time(c) for _, b, c in evs8) / len(evs8)
 
     # end to end through the public call with host buffers (pinned), copies inside the timed region.
@@ -370,7 +382,7 @@ def main():
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         pipelined(args.steps, t_start, t_end)
         torch.cuda.synchronize()
-        e_pipe = t_start.elapsed_time(t_end) / args.steps
+        e_pipe = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world, dev)
         # serial form
         e_ms = []
         for it in range(args.warmup + args.steps):
@@ -387,12 +399,12 @@ def main():
             if it >= args.warmup:
                 e_ms.append((a, c))
         torch.cuda.synchronize()
-        e_serial = sum(a.elapsed_time(c) for a, c in e_ms) / len(e_ms)
-        e2e = {"value": world * flops / (e_pipe * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_pipe,
+        e_serial = max_over_ranks(sum(a.elapsed_time(c) for a, c in e_ms) / len(e_ms), world, dev)
+        e2e = {"value": whole_job_tflops(flops, world, e_pipe), "unit": "TFLOP/s", "ms_per_step": e_pipe,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "form": "copies pipelined with compute over two streams (inputs larger than L2, rewritten by "
                        "each step's copy)",
-               "serial": {"value": world * flops / (e_serial * 1e-3) / 1e12, "ms_per_step": e_serial}}
+               "serial": {"value": whole_job_tflops(flops, world, e_serial), "ms_per_step": e_serial}}
 
     if rank != 0:
         return
@@ -425,10 +437,10 @@ def main():
         "clocks": clk,
         "quant_ms": sum(quant_ms) / len(quant_ms),
         "attn_ms": attn_avg,
-        "p_terms2": {"ms_per_step": ms2, "attn_ms": attn2, "value": world * flops / (ms2 * 1e-3) / 1e12},
-        "mxfp8_o": {"ms_per_step": ms8, "attn_ms": attn8, "value": world * flops / (ms8 * 1e-3) / 1e12},
+        "p_terms2": {"ms_per_step": ms2, "attn_ms": attn2, "value": whole_job_tflops(flops, world, ms2)},
+        "mxfp8_o": {"ms_per_step": ms8, "attn_ms": attn8, "value": whole_job_tflops(flops, world, ms8)},
         "bwd": {"bwd_ms": bwd_avg, "fwd_bwd_ms": ms_per_step + bwd_avg,
-                "tflops": world * 2.5 * flops / (bwd_avg * 1e-3) / 1e12,
+                "tflops": whole_job_tflops(2.5 * flops, world, bwd_avg),
                 "note": "backward on decoded operands, BF16 MMAs; FLOPs = 2.5 x forward"},
         "wall_s_timed_region": t_wall,
     }
