@@ -18,7 +18,8 @@
 //   warps 4-11  softmax: each warp owns 16 query rows (TMEM 16x256b shape: a row's keys spread over
 //               a quad of lanes, reductions are quad shuffles); then the epilogue, where warps 4+q
 //               and 8+q store the two 64-column halves of rows 32q..32q+31.
-// TMEM (512 columns): S[0] 0-127, S[1] 128-255, O 256-383, scale factors from 384.
+// TMEM (512 columns): S[0] 0-127, S[1] 128-255, O 256-383, scale factors 384-411, Q 416-447 (the
+// QK MMA reads Q from tensor memory and only K from shared memory).
 // P (E4M3, 32 columns per term) is written over the S buffer it came from; the own-block BF16 P
 // goes to the other S buffer.
 #include <cstdint>
@@ -77,7 +78,8 @@ enum Bar : uint32_t {
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
 // TMEM column map
-constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_SFQ = 384, T_SFK = 388, T_SFV = 396, T_SFP = 404;
+constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_SFQ = 384, T_SFK = 388, T_SFV = 396, T_SFP = 404,
+                   T_Q = 416;   // Q bytes (128 rows x 128 B = 32 columns), the QK MMA's A operand
 
 // Softmax weights are p' = 2^(x - m_used + P_SHIFT) with x - m_used <= RESCALE_LOG2, so
 // p' < 2^8.8 = 445.7 < 448.  P scale bytes: term 0 holds p' (scale 2^-P_SHIFT), term 1 the
@@ -215,6 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (ok) {
         tc_fence_after();
         tc_cp_32x128b_warpx4(tmem + T_SFQ, desc_sf_block(sbase + OFF_SFQ));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {   // Q into TMEM, 32 bytes of each row per copy
+          asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(tmem + T_Q + 8 * kk), "l"(dQ + 2 * kk)
+                       : "memory");
+        }
         tc_cp_32x128b_warpx4(tmem + T_SFP, desc_sf_block(sbase + OFF_SFP));
         tc_cp_32x128b_warpx4(tmem + T_SFP + 4, desc_sf_block(sbase + OFF_SFP + 512));
       }
@@ -232,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tc_cp_32x128b_warpx4(tmem + T_SFV + 4 * sb, dSFV + (uint64_t)(st * 32));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8_ss(tS[sb], dQ + 2 * kk,
+            mma_mxf8_ts(tS[sb], tmem + T_Q + 8 * kk,
                         dK + (uint64_t)(st * (BN * HD / 16) + 2 * kk), idesc_mxf8(BM, BN, kk, kk),
                         tmem + T_SFQ, tmem + T_SFK + 4 * sb, kk > 0 ? 1u : 0u);
           }
