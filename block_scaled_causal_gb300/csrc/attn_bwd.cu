@@ -39,6 +39,9 @@ constexpr uint32_t ATOM = 128 * 128;   // one 128-row x 128-byte swizzle block (
 // TMEM columns: S, dP and two accumulators.  In the dK/dV kernel the scale factors of the S MMA
 // sit at the start of dP's columns; dP is issued only once the S MMA has completed.
 constexpr uint32_t T_S = 0, T_DP = 128, T_ACC0 = 256, T_ACC1 = 384;
+// In the dQ kernel the query tile's operands stay in tensor memory: Q bytes (32 columns) and dO
+// (BF16, 64 columns), the A operands of the S and dP MMAs.
+constexpr uint32_t T_QT = 400, T_DOT = 432;
 
 enum Site : int { W_KV = 0x20, W_QD, W_MMA1, W_MMA2, W_MMA3, W_DO };
 
@@ -193,6 +196,18 @@ __device__ __forceinline__ void mma_s(uint32_t tmem, uint32_t t_sf, uint32_t q8,
   for (int kk = 0; kk < 4; ++kk) {
     mma_mxf8_ss(tmem + T_S, desc_kmajor_sw128(q8 + kk * 32), desc_kmajor_sw128(k8 + kk * 32),
                 idesc_mxf8(BM, BN, kk, kk), tmem + t_sf, tmem + t_sf + 4, kk > 0 ? 1u : 0u);
+  }
+}
+
+// S = Qh Kh^T with the Q bytes in tensor memory (columns t_q..t_q+31).
+__device__ __forceinline__ void mma_s_tq(uint32_t tmem, uint32_t t_sf, uint32_t t_q, uint32_t k8, uint32_t sfq,
+                                         uint32_t sfk) {
+  tc_cp_32x128b_warpx4(tmem + t_sf, desc_sf_block(sfq));
+  tc_cp_32x128b_warpx4(tmem + t_sf + 4, desc_sf_block(sfk));
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    mma_mxf8_ts(tmem + T_S, tmem + t_q + 8 * kk, desc_kmajor_sw128(k8 + kk * 32), idesc_mxf8(BM, BN, kk, kk),
+                tmem + t_sf, tmem + t_sf + 4, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -541,6 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   row_stats(a, b, hq, it, lse2, dlt);
   ok = cta_all(mbar_wait(bar(QB_QD), 0, ctl, W_QD));
   const bool qd_seen = ok;
+  if (leader && ok) {   // the Q bytes and dO into tensor memory, once
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) tc_cp_128x256b(tmem + T_QT + 8 * kk, desc_kmajor_sw128(sbase + QQ_Q8 + kk * 32));
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      tc_cp_128x256b(tmem + T_DOT + 8 * s, desc_kmajor_sw128(sbase + QQ_DO + (s >> 2) * ATOM + (s & 3) * 32));
+  }
 
   const RowView rv = row_view();
   for (int jt = 0; jt <= it; ++jt) {
@@ -561,8 +584,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     if (leader && ok) {
-      mma_s(tmem, T_ACC1, sbase + QQ_Q8, sbase + QQ_K8 + st * 16384, sbase + QQ_SFQ, sbase + QQ_SFK + st * 512);
-      mma_bf16_k128<false, false>(tmem + T_DP, sbase + QQ_DO, sbase + QQ_V, false);   // dP = dO V^T
+      mma_s_tq(tmem, T_ACC1, T_QT, sbase + QQ_K8 + st * 16384, sbase + QQ_SFQ, sbase + QQ_SFK + st * 512);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {   // dP = dO V^T, dO from tensor memory
+        mma_f16_ts(tmem + T_DP, tmem + T_DOT + 8 * s,
+                   desc_kmajor_sw128(sbase + QQ_V + (s >> 2) * ATOM + (s & 3) * 32), idesc_bf16(BM, BN),
+                   s > 0 ? 1u : 0u);
+      }
       tc_commit(bar(QB_MMA1));
     }
     if (ok) ok = mbar_wait(bar(QB_MMA1), par, ctl, W_MMA1);

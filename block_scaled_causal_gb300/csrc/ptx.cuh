@@ -149,6 +149,12 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
+// 128 rows x 32 bytes of an operand tile in shared memory (matrix descriptor, e.g. one K = 32 FP8 or
+// K = 16 BF16 slice of a K-major tile) into 8 TMEM columns, row m in lane m: the A-operand layout of
+// an MMA that reads A from tensor memory.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 
 // Block-scaled MXFP8 MMA (E4M3 x E4M3, UE8M0 scales per 32 along K), A and B from shared memory.
 __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
