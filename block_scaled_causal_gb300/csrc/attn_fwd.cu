@@ -219,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_cp_32x128b_warpx4(tmem + T_SFQ, desc_sf_block(sbase + OFF_SFQ));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {   // Q into TMEM, 32 bytes of each row per copy
-          tc_cp_128x256b(tmem + T_Q + 8 * kk, dQ + 2 * kk);
+          asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(tmem + T_Q + 8 * kk), "l"(dQ + 2 * kk)
+                       : "memory");
         }
         tc_cp_32x128b_warpx4(tmem + T_SFP, desc_sf_block(sbase + OFF_SFP));
         tc_cp_32x128b_warpx4(tmem + T_SFP + 4, desc_sf_block(sbase + OFF_SFP + 512));
