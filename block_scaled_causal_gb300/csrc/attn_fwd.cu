@@ -13,8 +13,10 @@
 // Warp roles (384 threads):
 //   warp 0      TMA producer: Q tile + scales once; K, V (columnwise, transposed) tiles + scales
 //               through a 4-stage ring; the own-block token-normalised V tile once.
-//   warp 1      allocates TMEM; lane 0 issues tcgen05.cp (scale factors) and tcgen05.mma.
-//   warps 2-3   decode the token-normalised V tile to BF16 (exact) in the MMA operand layout.
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.cp (scale factors, Q) and tcgen05.mma.
+//   warp 2      decodes the token-normalised V tile to BF16 (exact) in the MMA operand layout.
+//   warp 3      forwarder: turns each K/V stage's mbarrier completion into a named-barrier
+//               generation for warp 1.
 //   warps 4-11  softmax: each warp owns 16 query rows (TMEM 16x256b shape: a row's keys spread over
 //               a quad of lanes, reductions are quad shuffles); then the epilogue, where warps 4+q
 //               and 8+q store the two 64-column halves of rows 32q..32q+31.
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tma_load_4d(sbase + OFF_Q, &a.tm_q, bar(B_Q_FULL), 0, hq, t * BM, b);
       bulk_load(sbase + OFF_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + t) * 512, 512, bar(B_Q_FULL));
       if (own_split) {
-        // the own-block tile of the token-normalised V, decoded early by warps 2-3
+        // the own-block tile of the token-normalised V, decoded early by warp 2
         prefetch_tensormap(&a.tm_vtn);
         // amplitudes of the tile's keys that exist (a multiple of 32); the decode zeroes the rest
         const uint32_t namp = (uint32_t)min(BN, a.S - t * BN);
