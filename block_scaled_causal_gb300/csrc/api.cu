@@ -42,8 +42,9 @@ bsc_status check_shape(int B, int S, int H, int D, int layout, bool* empty) {
     return BSC_OK;
   }
   if (D != 128 || S % 32 != 0) return BSC_ERR_UNSUPPORTED;
-  // every index the kernels form fits in 64 bits; the grids must fit their limits
-  if ((long long)B * H * ((S + 127) / 128) >= (1LL << 31)) return BSC_ERR_UNSUPPORTED;
+  // every index the kernels form fits in 64 bits; the grids (one CTA per 64 tokens of a (b, h) plane
+  // at most) must fit their limits
+  if ((long long)B * H * ((S + 63) / 64) >= (1LL << 31)) return BSC_ERR_UNSUPPORTED;
   return BSC_OK;
 }
 
@@ -210,6 +211,8 @@ bsc_status mxfp8_quantize_qkv(const bsc_qkv_quant_params* p, bsc_stream_t stream
   if (!empty && p->Hkv == 0) return BSC_ERR_SHAPE;
   if (empty) return BSC_OK;
   if (p->Hq % p->Hkv != 0) return BSC_ERR_SHAPE;
+  // one launch: V tiles plus Q's and K's 64-token chunks
+  if ((long long)p->B * (p->Hq + 2LL * p->Hkv) * ((p->S + 63) / 64) >= (1LL << 31)) return BSC_ERR_UNSUPPORTED;
   const bool col = p->v_e4m3_t != nullptr || p->v_sc != nullptr;
   const bool tn = p->vtn_e4m3 != nullptr || p->vtn_sc != nullptr;
   if (!p->q || !p->k || !p->v || !p->q_e4m3 || !p->q_sc || !p->k_e4m3 || !p->k_sc) return BSC_ERR_NULL;
