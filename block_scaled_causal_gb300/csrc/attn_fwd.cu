@@ -85,11 +85,14 @@ constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_SFQ = 384, T_SFK = 388, T_
 
 // Softmax weights are p' = 2^(x - m_used + P_SHIFT) with x - m_used <= RESCALE_LOG2, so
 // p' < 2^8.8 = 445.7 < 448.  P scale bytes: term 0 holds p' (scale 2^-P_SHIFT), term 1 the
-// residual * 16 (scale 2^-(P_SHIFT+4)).
-constexpr float P_SHIFT = 8.0f;
-constexpr float RESCALE_LOG2 = 0.8f;
-constexpr uint8_t SFP_TERM0 = 127 - 8;
-constexpr uint8_t SFP_TERM1 = 127 - 12;
+// residual * 16 (scale 2^-(P_SHIFT+4)).  P_SHIFT + RESCALE_LOG2 = 8.8 fixes the largest weight; a
+// smaller shift lets the running maximum lag further behind the row's scores before O must be
+// rescaled (each rescale stalls the warp on the previous P.V), at the cost of E4M3 underflow for
+// weights more than 2^-(P_SHIFT + 9.5) below the running maximum.
+constexpr float P_SHIFT = 6.0f;
+constexpr float RESCALE_LOG2 = 2.8f;
+constexpr uint8_t SFP_TERM0 = 127 - 6;
+constexpr uint8_t SFP_TERM1 = 127 - 10;
 
 // wait-site codes reported through the device status word
 enum Site : int {
