@@ -136,6 +136,13 @@ __device__ __forceinline__ void row_stats_tiles(const BwdArgs& a, int it, const 
 
 // E4M3 tile [row][d] (TMA, 128-byte swizzle) with row-atom scales -> BF16 [row][d].  Rows at or
 // past `nrows` become 0.
+// Row position of key r in a decoded K tile that dQ's MMA reads against dS held in tensor memory:
+// inside each 16-key group, key 8b + 2a + e (a < 4, b, e < 2) goes to row 4a + 2b + e, the K order
+// of dS written with the 16x256b store (see dq_store_ds).
+__device__ __forceinline__ int ds_key_row(int r) {
+  return (r & ~15) | (((r >> 1) & 3) << 2) | (((r >> 3) & 1) << 1) | (r & 1);
+}
+template <bool PERM = false>
 __device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* sc_atom, uint8_t* dst, int nrows) {
   constexpr int kUnits = BM * (HD / 8) / kThreads;   // 8-element units per thread
   uint2 bytes[kUnits];
@@ -149,7 +156,7 @@ __device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* 
 #pragma unroll
   for (int u = 0; u < kUnits; ++u) {
     const int unit = threadIdx.x + u * kThreads, r = unit >> 4, d0 = (unit & 15) * 8;
-    *reinterpret_cast<uint4*>(dst + bf_off(r, d0)) = decode8(bytes[u], sc[u]);
+    *reinterpret_cast<uint4*>(dst + bf_off(PERM ? ds_key_row(r) : r, d0)) = decode8(bytes[u], sc[u]);
   }
 }
 // Token-normalised V bytes [key][d] (TMA, no swizzle) with one amplitude per key -> BF16 [key][d].
@@ -269,6 +276,24 @@ __device__ __forceinline__ void store_rows(uint8_t* tile, const RowView& rv, con
     *reinterpret_cast<uint32_t*>(tile + bf_off(rv.ra, key)) = pack_bf16x2(x[4 * k], x[4 * k + 1]);
     *reinterpret_cast<uint32_t*>(tile + bf_off(rv.rb, key)) = pack_bf16x2(x[4 * k + 2], x[4 * k + 3]);
   }
+}
+
+// dS as BF16 into tensor memory (64 columns from t_ds), the A operand of dQ += dS K: register
+// 4c + 2rr + b of the 16x256b store (row ra or rb for rr = 0, 1; column 8c + 2qd + b) holds the
+// keys 16c + 8b + 2qd and the next, so column 8c + 2qd + b carries K positions 16c + 4qd + 2b + e
+// for keys 16c + 8b + 2qd + e; the decoded K tile's rows use the same order (ds_key_row).
+__device__ __forceinline__ void dq_store_ds(uint32_t t_ds, const RowView& rv, const float (&ds)[64]) {
+  uint32_t w[32];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int k = 2 * c + b;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) w[4 * c + 2 * rr + b] = pack_bf16x2(ds[4 * k + 2 * rr], ds[4 * k + 2 * rr + 1]);
+    }
+  }
+  tmem_st16x256_x8(t_ds + rv.lane_off, w);
 }
 
 // Epilogue: an accumulator (128 rows x 128 columns fp32 in TMEM) times `mul` -> BF16 rows of a
@@ -484,10 +509,9 @@ constexpr uint32_t QQ_Q8 = 0;                       // Q bytes [q][d], swizzled
 constexpr uint32_t QQ_DO = QQ_Q8 + 16384;           // dO bf16 [q][d]
 constexpr uint32_t QQ_K8 = QQ_DO + 32768;           // 2 stages: K bytes [key][d], swizzled
 constexpr uint32_t QQ_VN8 = QQ_K8 + 2 * 16384;      // 2 stages: token-normalised V bytes [key][d]
-constexpr uint32_t QQ_K = QQ_VN8 + 2 * 16384;       // K bf16 [key][d]
+constexpr uint32_t QQ_K = QQ_VN8 + 2 * 16384;       // K bf16 [key][d], rows in the order of ds_key_row
 constexpr uint32_t QQ_V = QQ_K + 32768;             // V bf16 [key][d]
-constexpr uint32_t QQ_DS = QQ_V + 32768;            // dS bf16 [q][key]
-constexpr uint32_t QQ_SFQ = QQ_DS + 32768;
+constexpr uint32_t QQ_SFQ = QQ_V + 32768;
 constexpr uint32_t QQ_SFK = QQ_SFQ + 512;           // 2 stages
 constexpr uint32_t QQ_AMP = QQ_SFK + 1024;          // 2 stages of 128
 constexpr uint32_t QQ_LSE = QQ_AMP + 256;
@@ -577,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     if (ok) ++kv_seen[st];
     if (ok) {
       decode_vt(smem + QQ_VN8 + st * 16384, smem + QQ_AMP + st * 128, smem + QQ_V, nkeys);
-      decode_rows(smem + QQ_K8 + st * 16384, smem + QQ_SFK + st * 512, smem + QQ_K, nkeys);
+      decode_rows<true>(smem + QQ_K8 + st * 16384, smem + QQ_SFK + st * 512, smem + QQ_K, nkeys);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -600,14 +624,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       float p[64], ds[64];
       compute_p(tmem, rv, lse2, a.scale_log2e, jt == it, p);
       compute_ds(tmem, rv, dlt, p, ds);
-      store_rows(smem + QQ_DS, rv, ds);
+      dq_store_ds(tmem + T_S, rv, ds);   // over S, read into registers above
+      tmem_st_wait();
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (leader && ok) {
-      mma_bf16_k128<false, true>(tmem + T_ACC0, sbase + QQ_DS, sbase + QQ_K, jt > 0);   // dQ += dS K
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {   // dQ += dS K, dS from tensor memory
+        mma_f16_ts(tmem + T_ACC0, tmem + T_S + 8 * s, smem_desc(sbase + QQ_K + s * 2048, ATOM, 1024, 2),
+                   idesc_bf16(BM, BN) | (1u << 16), (jt > 0 || s > 0) ? 1u : 0u);
+      }
       tc_commit(bar(QB_MMA2));
     }
     if (ok) ok = mbar_wait(bar(QB_MMA2), par, ctl, W_MMA2);
