@@ -15,10 +15,11 @@
 // S = Qh Kh^T is one block-scaled E4M3 MMA on the MXFP8 bytes and scales (exact products); dP, dV,
 // dK and dQ are BF16 MMAs.  Every tile sits in shared memory in its natural orientation
 // ([row][column], 64-column blocks with the 128-byte swizzle); the products that contract over
-// its rows (P^T dO, dS^T Q, dS K) read it as an MN-major operand, so nothing is transposed.  The
-// next iteration's copies are issued while the current one computes; the phases of an iteration
-// run in turn, all threads taking part, thread 0 issuing the copies and MMAs.  Every wait is
-// bounded.
+// its rows (P^T dO, dS^T Q, dS K) read it as an MN-major operand, so nothing is transposed.  In
+// the dQ kernel the query tile's Q bytes and dO, and each iteration's dS, are the A operands of
+// their MMAs from tensor memory.  The next iteration's copies are issued while the current one
+// computes; the phases of an iteration run in turn, all threads taking part, thread 0 issuing the
+// copies and MMAs.  Every wait is bounded.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
