@@ -235,20 +235,19 @@ def main():
     q_cpu, k_cpu, v_cpu = I.make_qkv(w)
     q, k, v = q_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev)
     B, S, Hq, Hkv, D = w.B, w.S, w.Hq, w.Hkv, w.D
-    T = S // 128
     u8 = dict(dtype=torch.uint8, device=dev)
     qq = torch.empty(q.shape, **u8)
-    qs = torch.empty((B, Hq, T, 512), **u8)
+    qs = torch.empty((B, Hq, S, D // 32), **u8)
     kq = torch.empty(k.shape, **u8)
-    ks = torch.empty((B, Hkv, T, 512), **u8)
+    ks = torch.empty((B, Hkv, S, D // 32), **u8)
     vt = torch.empty((B, Hkv, D, S), **u8)
-    vsc = torch.empty((B, Hkv, T, 512), **u8)
+    vsc = torch.empty((B, Hkv, S // 32, D), **u8)
     vtn = torch.empty(v.shape, **u8)
     vtn_sc = torch.empty((B, Hkv, S), **u8)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
     o8 = torch.empty(q.shape, **u8)
-    o8_sc = torch.empty((B, Hq, T, 512), **u8)
+    o8_sc = torch.empty((B, Hq, S, D // 32), **u8)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)   # 256 MB > L2
     stream = torch.cuda.current_stream(dev)
 

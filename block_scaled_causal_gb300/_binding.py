@@ -145,12 +145,11 @@ def _require(x: torch.Tensor, dtype, name):
 
 
 def mxfp8_quantize_qk_rowwise(x, layout=BSHD, out=None, out_sc=None, stream=None):
-    """Returns (E4M3 bytes shaped like x, row-atom scales [B, H, ceil(S/128), 512])."""
+    """Returns (E4M3 bytes shaped like x, scales [B, H, S, D/32])."""
     _require(x, torch.bfloat16, "x")
     B, S, H, D = _bshd_dims(x, layout)
     out = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if out is None else out
-    out_sc = torch.empty((B, H, (S + 127) // 128, 512), dtype=torch.uint8, device=x.device) \
-        if out_sc is None else out_sc
+    out_sc = torch.empty((B, H, S, D // 32), dtype=torch.uint8, device=x.device) if out_sc is None else out_sc
     _check(lib.mxfp8_quantize_qk_rowwise(_ptr(x), B, S, H, D, layout, _ptr(out), _ptr(out_sc), _stream(stream)))
     return out, out_sc
 
@@ -160,7 +159,7 @@ def _v_outputs(v, B, S, H, D, col, tn):
     r = []
     if col:
         r += [torch.empty((B, H, D, S), dtype=torch.uint8, device=dev),
-              torch.empty((B, H, (S + 127) // 128, 512), dtype=torch.uint8, device=dev)]
+              torch.empty((B, H, S // 32, D), dtype=torch.uint8, device=dev)]
     if tn:
         r += [torch.empty(v.shape, dtype=torch.uint8, device=dev),
               torch.empty((B, H, S), dtype=torch.uint8, device=dev)]
@@ -168,7 +167,7 @@ def _v_outputs(v, B, S, H, D, col, tn):
 
 
 def mxfp8_quantize_v_colwise(v, layout=BSHD, stream=None):
-    """Returns (E4M3 bytes of V transposed [B, H, D, S], column-atom scales [B, H, ceil(S/128), 512])."""
+    """Returns (E4M3 bytes of V transposed [B, H, D, S], scales [B, H, S/32, D])."""
     _require(v, torch.bfloat16, "v")
     B, S, H, D = _bshd_dims(v, layout)
     vt, vsc = _v_outputs(v, B, S, H, D, True, False)
@@ -195,7 +194,7 @@ def mxfp8_quantize_v_fused(v, layout=BSHD, out=None, stream=None):
     return vt, vsc, vtn, vtn_sc
 
 
-def make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, softmax_scale, p_terms=1, leaky=0,
+def make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, softmax_scale, p_terms=2, leaky=0,
                      dev_status=None, wait_timeout_ms=0, debug_stall=0, o8=None, o_sc=None):
     B, S, Hq, D = _bshd_dims(q, layout)
     Hkv = _bshd_dims(k, layout)[2]
@@ -209,13 +208,14 @@ def make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, s
                          o_e4m3=0 if o8 is None else o8.data_ptr(), o_sc=0 if o_sc is None else o_sc.data_ptr())
 
 
-def mxfp8_causal_attn_fwd(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, layout=BSHD, softmax_scale=None, p_terms=1,
+def mxfp8_causal_attn_fwd(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, layout=BSHD, softmax_scale=None, p_terms=2,
                           leaky=0, o=None, lse=None, dev_status=None, wait_timeout_ms=0, debug_stall=0,
                           stream=None, o8_out=False, bf16_out=True, o8=None, o_sc=None):
     """Leak-free causal MXFP8 attention forward on quantised operands.
 
     Returns (O bf16, LSE fp32); with o8_out=True, (O bf16 or None, LSE, O E4M3 bytes laid out like
-    q, O row-atom scales [B, Hq, ceil(S/128), 512]).
+    q, O scales [B, Hq, S, D/32]).  p_terms: E4M3 terms of P for the completed blocks (2: the
+    tolerance-preserving default; 1: faster, one E4M3 rounding of P).
     """
     B, S, Hq, D = _bshd_dims(q, layout)
     if softmax_scale is None:
@@ -227,7 +227,7 @@ def mxfp8_causal_attn_fwd(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, layout=BSHD,
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if lse is None else lse
     if o8_out:
         o8 = torch.empty(q.shape, dtype=torch.uint8, device=q.device) if o8 is None else o8
-        o_sc = torch.empty((B, Hq, (S + 127) // 128, 512), dtype=torch.uint8, device=q.device) if o_sc is None else o_sc
+        o_sc = torch.empty((B, Hq, S, D // 32), dtype=torch.uint8, device=q.device) if o_sc is None else o_sc
     else:
         o8 = o_sc = None
     p = make_attn_params(q, q_sc, k, k_sc, v_t, v_sc, vtn, vtn_sc, o, lse, layout, softmax_scale, p_terms, leaky,
@@ -241,7 +241,7 @@ def bsc_read_device_status(dev_status, stream=None):
     return lib.bsc_read_device_status(_ptr(dev_status), _stream(stream))
 
 
-def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=1, leaky=0, o=None, lse=None, stream=None,
+def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=2, leaky=0, o=None, lse=None, stream=None,
             o8_out=False, bf16_out=True):
     """The whole hot path on bf16 inputs: quantise Q, K rowwise, V columnwise + token-normalised,
     then the leak-free causal attention forward.  Returns (O bf16, LSE fp32); `o` and `lse` may be
@@ -274,28 +274,27 @@ def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softma
     return dq, dk, dv
 
 
-def forward_backward(q, k, v, do, layout=BSHD, softmax_scale=None, stream=None):
-    """Forward (one E4M3 term for P) then the backward on decoded operands; returns
-    (O, LSE, dQ, dK, dV)."""
+def forward_backward(q, k, v, do, layout=BSHD, softmax_scale=None, p_terms=2, stream=None):
+    """Forward then the backward on decoded operands; returns (O, LSE, dQ, dK, dV)."""
     qq, qs, kq, ks, vt, vsc, vtn, vtn_sc = mxfp8_quantize_qkv(q, k, v, layout, stream=stream)
-    o, lse = mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, stream=stream)
+    o, lse = mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, layout, softmax_scale, p_terms,
+                                   stream=stream)
     dq, dk, dv = bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o, lse, do, layout, softmax_scale, stream=stream)
     return o, lse, dq, dk, dv
 
 
 def mxfp8_quantize(kind, x, layout=BSHD, rule=SCALE_FLOOR, stream=None):
     """Any quantisation with a chosen scale rule.  Returns the outputs of the matching call:
-    (bytes, row atoms) for QUANT_ROWWISE, (V^T bytes, column atoms) for QUANT_V_COLWISE,
+    (bytes, [B,H,S,D/32] scales) for QUANT_ROWWISE, (V^T bytes, [B,H,S/32,D] scales) for QUANT_V_COLWISE,
     (token-normalised bytes, amplitudes) for QUANT_V_TOKEN_NORM, all four for QUANT_V_FUSED."""
     _require(x, torch.bfloat16, "x")
     B, S, H, D = _bshd_dims(x, layout)
-    T = (S + 127) // 128
     u8 = dict(dtype=torch.uint8, device=x.device)
     e4m3 = sc = vtn = vtn_sc = None
     if kind == QUANT_ROWWISE:
-        e4m3, sc = torch.empty(x.shape, **u8), torch.empty((B, H, T, 512), **u8)
+        e4m3, sc = torch.empty(x.shape, **u8), torch.empty((B, H, S, D // 32), **u8)
     if kind in (QUANT_V_COLWISE, QUANT_V_FUSED):
-        e4m3, sc = torch.empty((B, H, D, S), **u8), torch.empty((B, H, T, 512), **u8)
+        e4m3, sc = torch.empty((B, H, D, S), **u8), torch.empty((B, H, S // 32, D), **u8)
     if kind in (QUANT_V_TOKEN_NORM, QUANT_V_FUSED):
         vtn, vtn_sc = torch.empty(x.shape, **u8), torch.empty((B, H, S), **u8)
     p = QuantParams(kind=kind, x=x.data_ptr(), B=B, S=S, H=H, D=D, layout=layout, rule=rule,
@@ -318,12 +317,11 @@ def mxfp8_quantize_qkv(q, k, v, layout=BSHD, rule=SCALE_FLOOR, token_norm=True, 
     Hkv = _bshd_dims(k, layout)[2]
     if tuple(k.shape) != tuple(v.shape):
         raise ValueError("k and v must have the same shape")
-    T = (S + 127) // 128
     if out is None:
         u8 = dict(dtype=torch.uint8, device=q.device)
-        out = (torch.empty(q.shape, **u8), torch.empty((B, Hq, T, 512), **u8),
-               torch.empty(k.shape, **u8), torch.empty((B, Hkv, T, 512), **u8),
-               torch.empty((B, Hkv, D, S), **u8), torch.empty((B, Hkv, T, 512), **u8),
+        out = (torch.empty(q.shape, **u8), torch.empty((B, Hq, S, D // 32), **u8),
+               torch.empty(k.shape, **u8), torch.empty((B, Hkv, S, D // 32), **u8),
+               torch.empty((B, Hkv, D, S), **u8), torch.empty((B, Hkv, S // 32, D), **u8),
                torch.empty(v.shape, **u8) if token_norm else None,
                torch.empty((B, Hkv, S), **u8) if token_norm else None)
     qq, qs, kq, ks, vt, vsc, vtn, vtn_sc = out

@@ -1,4 +1,5 @@
 // C-ABI entry points: argument checks, tensor-map creation, launches.  See include/bsc.h.
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -131,7 +132,7 @@ bsc_status quant_v_common(const void* v, int B, int S, int H, int D, bsc_layout 
 
 extern "C" {
 
-int bsc_abi_version(void) { return 2; }
+int bsc_abi_version(void) { return 3; }
 
 const char* bsc_status_string(bsc_status s) {
   switch (s) {
@@ -255,6 +256,8 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
   if (p->Hq % p->Hkv != 0) return BSC_ERR_SHAPE;
   if (p->p_terms != 1 && p->p_terms != 2) return BSC_ERR_UNSUPPORTED;
   if (p->leaky != 0 && p->leaky != 1) return BSC_ERR_UNSUPPORTED;
+  // the kernel takes row maxima of the raw scores before scaling: a positive, finite scale only
+  if (!(std::isfinite(p->softmax_scale) && p->softmax_scale > 0.f)) return BSC_ERR_UNSUPPORTED;
   const bool own = p->leaky == 0;
   if (!p->q || !p->q_sc || !p->k || !p->k_sc || !p->v_t || !p->v_sc || !p->lse) return BSC_ERR_NULL;
   if (!p->o && !p->o_e4m3) return BSC_ERR_NULL;
@@ -273,10 +276,10 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
       !encode_tokens_map(&a.tm_k, p->k, p->B, p->S, p->Hkv, p->layout, true) ||
       !encode_vt_map(&a.tm_v, p->v_t, (long long)p->B * p->Hkv * 128, p->S))
     return BSC_ERR_CUDA;
-  if (own && !encode_tokens_map(&a.tm_vtn, p->vtn, p->B, p->S, p->Hkv, p->layout, false)) return BSC_ERR_CUDA;
   a.q_sc = p->q_sc;
   a.k_sc = p->k_sc;
   a.v_sc = p->v_sc;
+  a.vtn = own ? p->vtn : nullptr;
   a.vtn_sc = own ? p->vtn_sc : nullptr;
   a.o = p->o;
   a.o8 = p->o_e4m3;
@@ -305,6 +308,7 @@ bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
   if (!empty && p->Hkv == 0) return BSC_ERR_SHAPE;
   if (empty) return BSC_OK;
   if (p->Hq % p->Hkv != 0) return BSC_ERR_SHAPE;
+  if (!(std::isfinite(p->softmax_scale) && p->softmax_scale > 0.f)) return BSC_ERR_UNSUPPORTED;
   if (!p->q || !p->q_sc || !p->k || !p->k_sc || !p->vtn || !p->vtn_sc || !p->o || !p->lse || !p->d_o || !p->dq ||
       !p->dk || !p->dv)
     return BSC_ERR_NULL;

@@ -36,6 +36,9 @@ constexpr int BN = 128;   // keys per tile
 constexpr int HD = 128;   // head dimension
 constexpr int kThreads = 256;
 constexpr uint32_t ATOM = 128 * 128;   // one 128-row x 128-byte swizzle block (64 BF16 columns)
+// dS in tensor memory (64 BF16 columns over S) and its K order (ds_key_row) cover one 128-key tile
+// in 16-key groups; the dQ MMA's K is that tile, its N the head dimension.
+static_assert(BN == 128 && HD == 128, "tile shapes assumed by the tensor-memory layouts");
 
 // TMEM columns: S, dP and two accumulators.  In the dK/dV kernel the scale factors of the S MMA
 // sit at the start of dP's columns; dP is issued only once the S MMA has completed.
@@ -60,9 +63,15 @@ __device__ __forceinline__ uint32_t bf_off(uint32_t row, uint32_t col) {
 __device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
   return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);   // 2^(sb-127)
 }
-// Row atom byte of (row, 32-element block) in a 512-byte scale atom.
-__device__ __forceinline__ uint32_t atom_byte(uint32_t row, uint32_t blk) {
-  return (row & 31u) * 16u + ((row >> 5) & 3u) * 4u + blk;
+// Compact rowwise scales of a 128-row tile (one 32-bit word per row, byte c for the 32-element
+// block c) -> the tensor-core scale-factor atom: row m's word at (m % 32) * 16 + (m / 32) * 4.
+// Rows at or past `nrows` get 0.  One warp; lane l writes the atom's 16-byte line l.
+__device__ __forceinline__ void rows_to_atom(const uint8_t* compact, uint8_t* atom, int nrows, int lane) {
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(compact);
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = lane + 32 * k < nrows ? src[lane + 32 * k] : 0u;
+  *reinterpret_cast<uint4*>(atom + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 // Eight E4M3 bytes (one uint2) * scale -> eight BF16 (one uint4); exact for in-range values.
 __device__ __forceinline__ uint4 decode8(uint2 bytes, float scale) {
@@ -135,8 +144,8 @@ __device__ __forceinline__ void row_stats_tiles(const BwdArgs& a, int it, const 
   }
 }
 
-// E4M3 tile [row][d] (TMA, 128-byte swizzle) with row-atom scales -> BF16 [row][d].  Rows at or
-// past `nrows` become 0.
+// E4M3 tile [row][d] (TMA, 128-byte swizzle) with compact row scales -> BF16 [row][d].  Rows at
+// or past `nrows` become 0.
 // Row position of key r in a decoded K tile that dQ's MMA reads against dS held in tensor memory:
 // inside each 16-key group, key 8b + 2a + e (a < 4, b, e < 2) goes to row 4a + 2b + e, the K order
 // of dS written with the 16x256b store (see dq_store_ds).
@@ -144,7 +153,7 @@ __device__ __forceinline__ int ds_key_row(int r) {
   return (r & ~15) | (((r >> 1) & 3) << 2) | (((r >> 3) & 1) << 1) | (r & 1);
 }
 template <bool PERM = false>
-__device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* sc_atom, uint8_t* dst, int nrows) {
+__device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* sc_rows, uint8_t* dst, int nrows) {
   constexpr int kUnits = BM * (HD / 8) / kThreads;   // 8-element units per thread
   uint2 bytes[kUnits];
   float sc[kUnits];
@@ -152,7 +161,7 @@ __device__ __forceinline__ void decode_rows(const uint8_t* src8, const uint8_t* 
   for (int u = 0; u < kUnits; ++u) {   // every load first
     const int unit = threadIdx.x + u * kThreads, r = unit >> 4, d0 = (unit & 15) * 8;
     bytes[u] = *reinterpret_cast<const uint2*>(src8 + sw(r, d0));
-    sc[u] = r < nrows ? pow2_e8m0(sc_atom[atom_byte(r, d0 >> 5)]) : 0.f;
+    sc[u] = r < nrows ? pow2_e8m0(sc_rows[r * 4 + (d0 >> 5)]) : 0.f;
   }
 #pragma unroll
   for (int u = 0; u < kUnits; ++u) {
@@ -335,9 +344,11 @@ constexpr uint32_t KV_DO = KV_Q + 32768;      // dO bf16 [q][d]
 constexpr uint32_t KV_P = KV_DO + 32768;      // P bf16 [q][key] (the V bytes [key][d] before that)
 constexpr uint32_t KV_VN8 = KV_P;
 constexpr uint32_t KV_DS = KV_P + 32768;      // dS bf16 [q][key] (O bf16 [q][d] before that)
-constexpr uint32_t KV_SFQ = KV_DS + 32768;
-constexpr uint32_t KV_SFK = KV_SFQ + 512;
-constexpr uint32_t KV_AMP = KV_SFK + 512;
+constexpr uint32_t KV_SFQ = KV_DS + 32768;     // compact Q scales of the tile
+constexpr uint32_t KV_SFK = KV_SFQ + 512;      // compact K scales
+constexpr uint32_t KV_SFQA = KV_SFK + 512;     // the same as scale-factor atoms
+constexpr uint32_t KV_SFKA = KV_SFQA + 512;
+constexpr uint32_t KV_AMP = KV_SFKA + 512;
 constexpr uint32_t KV_STAT = KV_AMP + 128;    // [2 buffers][LSE | Dlt][128] floats
 constexpr uint32_t KV_LSE = KV_STAT + 2048;
 constexpr uint32_t KV_BAR = KV_LSE + 512;
@@ -385,9 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   auto hq_of = [&](int n) { return hk * g + n % g; };
   auto it_of = [&](int n) { return T - 1 - n / g; };
   auto load_q = [&](int n) {
-    mbar_arrive_expect_tx(bar(KB_Q), BM * HD + 512);
+    const uint32_t nr = (uint32_t)min(BM, a.S - it_of(n) * BM);
+    mbar_arrive_expect_tx(bar(KB_Q), BM * HD + 4 * nr);
     tma_load_4d(sbase + KV_Q8, &a.tm_q, bar(KB_Q), 0, hq_of(n), it_of(n) * BM, b);
-    bulk_load(sbase + KV_SFQ, a.q_sc + (((long long)b * a.Hq + hq_of(n)) * T + it_of(n)) * 512, 512, bar(KB_Q));
+    bulk_load(sbase + KV_SFQ, a.q_sc + (((long long)b * a.Hq + hq_of(n)) * a.S + (long long)it_of(n) * BM) * 4, 4 * nr,
+              bar(KB_Q));
   };
   // dO into its tile and O into the dS tile (read for the row statistics before dS is written)
   auto load_do = [&](int n) {
@@ -406,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 
   // this CTA's K and V tiles, and the first query tile
   if (leader) {
-    mbar_arrive_expect_tx(bar(KB_KV), 2 * BN * HD + 512 + (uint32_t)nkeys);
+    mbar_arrive_expect_tx(bar(KB_KV), 2 * BN * HD + 4 * (uint32_t)nkeys + (uint32_t)nkeys);
     tma_load_4d(sbase + KV_K8, &a.tm_k, bar(KB_KV), 0, hk, jt * BN, b);
-    bulk_load(sbase + KV_SFK, a.k_sc + (kv_plane * T + jt) * 512, 512, bar(KB_KV));
+    bulk_load(sbase + KV_SFK, a.k_sc + (kv_plane * a.S + (long long)jt * BN) * 4, 4 * (uint32_t)nkeys, bar(KB_KV));
     tma_load_4d(sbase + KV_VN8, &a.tm_vtn, bar(KB_KV), 0, hk, jt * BN, b);
     bulk_load(sbase + KV_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, (uint32_t)nkeys, bar(KB_KV));
     load_q(0);
@@ -417,7 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   q_issued = do_issued = 1;
   ok = cta_all(mbar_wait(bar(KB_KV), 0, ctl, W_KV));
   const bool kv_seen = ok;
-  if (ok) decode_vt(smem + KV_VN8, smem + KV_AMP, smem + KV_V, nkeys);
+  if (ok) {
+    if (threadIdx.x < 32) rows_to_atom(smem + KV_SFK, smem + KV_SFKA, nkeys, threadIdx.x);
+    decode_vt(smem + KV_VN8, smem + KV_AMP, smem + KV_V, nkeys);
+  }
   __syncthreads();   // the V bytes are read before P overwrites them
 
   const RowView rv = row_view();
@@ -429,14 +445,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     if (ok) ok = mbar_wait(bar(KB_Q), par, ctl, W_QD);
     ok = cta_all(ok);
     if (ok) ++q_seen;
-    if (ok) decode_rows(smem + KV_Q8, smem + KV_SFQ, smem + KV_Q, min(BM, a.S - it * BM));
+    if (ok) {
+      if (threadIdx.x < 32) rows_to_atom(smem + KV_SFQ, smem + KV_SFQA, min(BM, a.S - it * BM), threadIdx.x);
+      decode_rows(smem + KV_Q8, smem + KV_SFQ, smem + KV_Q, min(BM, a.S - it * BM));
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     // S first: its scale factors occupy dP's first columns until it has completed
     if (leader && ok) {
-      mma_s(tmem, T_DP, sbase + KV_Q8, sbase + KV_K8, sbase + KV_SFQ, sbase + KV_SFK);
+      mma_s(tmem, T_DP, sbase + KV_Q8, sbase + KV_K8, sbase + KV_SFQA, sbase + KV_SFKA);
       tc_commit(bar(KB_MMA1));
     }
     if (ok) ok = mbar_wait(bar(KB_MMA1), par, ctl, W_MMA1);
@@ -512,9 +531,11 @@ constexpr uint32_t QQ_K8 = QQ_DO + 32768;           // 2 stages: K bytes [key][d
 constexpr uint32_t QQ_VN8 = QQ_K8 + 2 * 16384;      // 2 stages: token-normalised V bytes [key][d]
 constexpr uint32_t QQ_K = QQ_VN8 + 2 * 16384;       // K bf16 [key][d], rows in the order of ds_key_row
 constexpr uint32_t QQ_V = QQ_K + 32768;             // V bf16 [key][d]
-constexpr uint32_t QQ_SFQ = QQ_V + 32768;
-constexpr uint32_t QQ_SFK = QQ_SFQ + 512;           // 2 stages
-constexpr uint32_t QQ_AMP = QQ_SFK + 1024;          // 2 stages of 128
+constexpr uint32_t QQ_SFQ = QQ_V + 32768;           // compact Q scales of the tile
+constexpr uint32_t QQ_SFK = QQ_SFQ + 512;           // 2 stages of compact K scales
+constexpr uint32_t QQ_SFQA = QQ_SFK + 1024;         // Q scale atom
+constexpr uint32_t QQ_SFKA = QQ_SFQA + 512;         // K scale atom of the current key tile
+constexpr uint32_t QQ_AMP = QQ_SFKA + 512;          // 2 stages of 128
 constexpr uint32_t QQ_LSE = QQ_AMP + 256;
 constexpr uint32_t QQ_DLT = QQ_LSE + 512;
 constexpr uint32_t QQ_BAR = QQ_DLT + 512;
@@ -560,9 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     const int st = j & 1;
     const uint32_t nk = (uint32_t)min(BN, a.S - j * BN);
     const uint32_t kb = bar(QB_KV0 + st);
-    mbar_arrive_expect_tx(kb, 2 * BN * HD + 512 + nk);
+    mbar_arrive_expect_tx(kb, 2 * BN * HD + 4 * nk + nk);
     tma_load_4d(sbase + QQ_K8 + st * 16384, &a.tm_k, kb, 0, hk, j * BN, b);
-    bulk_load(sbase + QQ_SFK + st * 512, a.k_sc + (kv_plane * T + j) * 512, 512, kb);
+    bulk_load(sbase + QQ_SFK + st * 512, a.k_sc + (kv_plane * a.S + (long long)j * BN) * 4, 4 * nk, kb);
     tma_load_4d(sbase + QQ_VN8 + st * 16384, &a.tm_vtn, kb, 0, hk, j * BN, b);
     bulk_load(sbase + QQ_AMP + st * 128, a.vtn_sc + kv_plane * a.S + (long long)j * BN, nk, kb);
   };
@@ -570,9 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   int kv_issued[2] = {0, 0}, kv_seen[2] = {0, 0};
 
   if (leader) {
-    mbar_arrive_expect_tx(bar(QB_QD), BM * HD + 512 + 2 * BM * HD);
+    const uint32_t nr = (uint32_t)min(BM, a.S - it * BM);
+    mbar_arrive_expect_tx(bar(QB_QD), BM * HD + 4 * nr + 2 * BM * HD);
     tma_load_4d(sbase + QQ_Q8, &a.tm_q, bar(QB_QD), 0, hq, it * BM, b);
-    bulk_load(sbase + QQ_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * T + it) * 512, 512, bar(QB_QD));
+    bulk_load(sbase + QQ_SFQ, a.q_sc + (((long long)b * a.Hq + hq) * a.S + (long long)it * BM) * 4, 4 * nr,
+              bar(QB_QD));
     tma_load_4d(sbase + QQ_DO, &a.tm_do, bar(QB_QD), 0, hq, it * BM, b);
     tma_load_4d(sbase + QQ_DO + ATOM, &a.tm_do, bar(QB_QD), 64, hq, it * BM, b);
     load_kv(0);
@@ -581,6 +604,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   row_stats(a, b, hq, it, lse2, dlt);
   ok = cta_all(mbar_wait(bar(QB_QD), 0, ctl, W_QD));
   const bool qd_seen = ok;
+  if (ok && threadIdx.x < 32) {
+    rows_to_atom(smem + QQ_SFQ, smem + QQ_SFQA, min(BM, a.S - it * BM), threadIdx.x);
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
   if (leader && ok) {   // the Q bytes and dO into tensor memory, once
     tc_fence_after();
 #pragma unroll
@@ -601,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     ok = cta_all(ok);
     if (ok) ++kv_seen[st];
     if (ok) {
+      if (threadIdx.x < 32) rows_to_atom(smem + QQ_SFK + st * 512, smem + QQ_SFKA, nkeys, threadIdx.x);
       decode_vt(smem + QQ_VN8 + st * 16384, smem + QQ_AMP + st * 128, smem + QQ_V, nkeys);
       decode_rows<true>(smem + QQ_K8 + st * 16384, smem + QQ_SFK + st * 512, smem + QQ_K, nkeys);
     }
@@ -609,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     if (leader && ok) {
-      mma_s_tq(tmem, T_ACC1, T_QT, sbase + QQ_K8 + st * 16384, sbase + QQ_SFQ, sbase + QQ_SFK + st * 512);
+      mma_s_tq(tmem, T_ACC1, T_QT, sbase + QQ_K8 + st * 16384, sbase + QQ_SFQA, sbase + QQ_SFKA);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {   // dP = dO V^T, dO from tensor memory
         mma_f16_ts(tmem + T_DP, tmem + T_DOT + 8 * s,
@@ -636,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
 #pragma unroll
       for (int s = 0; s < 8; ++s) {   // dQ += dS K, dS from tensor memory
         mma_f16_ts(tmem + T_ACC0, tmem + T_S + 8 * s, smem_desc(sbase + QQ_K + s * 2048, ATOM, 1024, 2),
-                   idesc_bf16(BM, BN) | (1u << 16), (jt > 0 || s > 0) ? 1u : 0u);
+                   idesc_bf16(BM, HD) | (1u << 16), (jt > 0 || s > 0) ? 1u : 0u);
       }
       tc_commit(bar(QB_MMA2));
     }

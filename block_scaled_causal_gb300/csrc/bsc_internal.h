@@ -34,14 +34,14 @@ struct AttnArgs {
   CUtensorMap tm_q;     // Q bytes, 4-D {D, Hq, S, B}, box {128,1,128,1}, 128-byte swizzle
   CUtensorMap tm_k;     // K bytes, 4-D {D, Hkv, S, B}, same box
   CUtensorMap tm_v;     // V columnwise bytes, 2-D {S, B*Hkv*D}, box {128,128}, 128-byte swizzle
-  CUtensorMap tm_vtn;   // token-normalised V bytes, 4-D like K, no swizzle
-  const uint8_t* q_sc;
-  const uint8_t* k_sc;
-  const uint8_t* v_sc;
-  const uint8_t* vtn_sc;
+  const uint8_t* q_sc;     // compact [B][Hq][S][4]
+  const uint8_t* k_sc;     // compact [B][Hkv][S][4]
+  const uint8_t* v_sc;     // compact [B][Hkv][S/32][128]
+  const uint8_t* vtn;      // token-normalised V bytes, K's layout (unused when leaky)
+  const uint8_t* vtn_sc;   // [B][Hkv][S]
   void* o;              // bf16 O, or nullptr
   uint8_t* o8;          // E4M3 O, or nullptr
-  uint8_t* o_sc;        // row atoms of the E4M3 O scales (with o8)
+  uint8_t* o_sc;        // compact [B][Hq][S][4] scales of the E4M3 O (with o8)
   float* lse;
   int32_t* dev_status;
   unsigned long long limit_ns;
@@ -61,8 +61,8 @@ struct BwdArgs {
   CUtensorMap tm_vtn;   // token-normalised V bytes, as in AttnArgs
   CUtensorMap tm_do;    // dO bf16, 4-D {D, Hq, S, B}, box {64,1,128,1}, 128-byte swizzle
   CUtensorMap tm_o;     // O bf16, same form as dO
-  const uint8_t* q_sc;
-  const uint8_t* k_sc;
+  const uint8_t* q_sc;  // compact [B][Hq][S][4]
+  const uint8_t* k_sc;  // compact [B][Hkv][S][4]
   const uint8_t* vtn_sc;
   const void* o;        // bf16 O of the forward, Q's layout
   const void* dO;       // bf16 dO, Q's layout

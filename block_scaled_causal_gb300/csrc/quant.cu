@@ -45,17 +45,12 @@ __device__ __forceinline__ uint2 quant8(const uint4& v, float inv, bool nonfinit
   return make_uint2(out[0], out[1]);
 }
 
-// Byte offset of row m's 32-bit scale word inside a 128-row scale atom (F8_128x4 order):
-// rows m and m + 32 sit in adjacent words of the same 16-byte line.
-__device__ __forceinline__ uint32_t atom_word_offset(uint32_t m) { return (m & 31u) * 16u + ((m >> 5) & 3u) * 4u; }
-
 // ------------------------------------------------------------------------------------------
 // Rowwise quantiser (Q, K): a CTA of 256 threads takes 64 consecutive tokens s0..s0+63 of one
 // (b, h) plane; a token row is 256 bytes = 16 threads x 16 bytes (8 elements) and a 32-element
 // block is 4 adjacent threads.  Each thread loads its four chunks (rows s0 + 16i + tid/16) before
-// converting any, so that 64 bytes per thread are in flight.  Scale words go to the atom layout,
-// T = ceil(S/128) atoms per (b, h):
-//   sc[((b*H + h) * T + s/128) * 512 + (s%32)*16 + ((s%128)/32)*4 + c],  c = d / 32.
+// converting any, so that 64 bytes per thread are in flight.  Scales are compact: the four scale
+// bytes of token s (blocks c = d/32) form one 32-bit word at sc[((b*H + h)*S + s)*4 + c].
 constexpr int RW_ROWS = 64;
 
 // `blk` = plane * ceil(S/64) + s-chunk.
@@ -77,7 +72,6 @@ __device__ __forceinline__ void rowwise_rows(const uint8_t* __restrict__ x, uint
     e[i] = base0 + (long long)s * row_stride + l16 * 8;
     v[i] = s < S ? __ldcs(reinterpret_cast<const uint4*>(x + e[i] * 2)) : make_uint4(0, 0, 0, 0);
   }
-  const int T = (S + 127) / 128;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int s = s0 + 16 * i + (tid >> 4);
@@ -93,8 +87,7 @@ __device__ __forceinline__ void rowwise_rows(const uint8_t* __restrict__ x, uint
     const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 8);
     const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 12);
     if (s < S && l16 == 0) {
-      const long long off = (plane * T + s / 128) * 512 + atom_word_offset((uint32_t)(s & 127));
-      *reinterpret_cast<uint32_t*>(sc + off) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      *reinterpret_cast<uint32_t*>(sc + (plane * S + s) * 4) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
     }
   }
 }
@@ -105,24 +98,11 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint8_t* __res
   rowwise_rows(x, q, sc, B, S, H, layout, rule, blockIdx.x);
 }
 
-// Rows S..T*128-1 of the last row atom of each (b, h) hold no token: their scale words are 0.
-__global__ void __launch_bounds__(128) pad_row_atoms_kernel(uint8_t* __restrict__ sc, int S) {
-  const int T = (S + 127) / 128;
-  const int s = (T - 1) * 128 + (int)threadIdx.x;
-  if (s >= S) {
-    const long long off = ((long long)blockIdx.x * T + (T - 1)) * 512 + atom_word_offset((uint32_t)(s & 127));
-    *reinterpret_cast<uint32_t*>(sc + off) = 0u;
-  }
-}
-
 // ------------------------------------------------------------------------------------------
 // V quantiser: one CTA per (b, h, 128-token tile), 256 threads (the last tile of a sequence may
 // hold fewer than 128 tokens, always whole 32-token blocks).  Produces either or both of
-//   * the columnwise copy, transposed, with the tokens of each aligned 32-token block in the order
-//     perm32 (the order the attention kernel's P operand uses, see bsc.h):
-//     vt[((b*H + h)*D + d)*S + 32*blk + x] = token 32*blk + perm32(x), with scale atoms
-//       vsc[((b*H + h)*T + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32],  T = ceil(S/128)
-//     (the bytes of blocks past S in the last atom are 0);
+//   * the columnwise copy, transposed: vt[((b*H + h)*D + d)*S + s], with compact scales, one byte
+//     per (b, h, 32-token block, d): vsc[((b*H + h)*(S/32) + s/32)*D + d];
 //   * the token-normalised copy in V's own layout with scales vtn_sc[(b*H + h)*S + s].
 constexpr int VQ_ROWS = 128;
 constexpr int VQ_PITCH = 256 + 16;   // bytes per staged token row
@@ -179,32 +159,29 @@ __device__ __forceinline__ void v_tile(const uint8_t* __restrict__ v, uint8_t* _
   float inv0, inv1;
   const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0, rule);
   const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1, rule);
-  // Byte slot s of the 32-token block holds token perm32(s) = 8*((s%8)/2) + 2*(s/8) + s%2: word i
-  // (slots 4i..4i+3) holds tokens k0, k0+1, k0+8, k0+9 with k0 = 16*(i%2) + 2*(i/2).
+  // word i of a column's 32-token block holds tokens 4i..4i+3 (natural order)
   uint32_t o0[8], o1[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int k0 = 16 * (i & 1) + 2 * (i >> 1);
+    const int k0 = 4 * i;
     uint32_t lo0 = cvt_e4m3x2(bf16_lo(w[k0]) * inv0, bf16_lo(w[k0 + 1]) * inv0);
-    uint32_t hi0 = cvt_e4m3x2(bf16_lo(w[k0 + 8]) * inv0, bf16_lo(w[k0 + 9]) * inv0);
+    uint32_t hi0 = cvt_e4m3x2(bf16_lo(w[k0 + 2]) * inv0, bf16_lo(w[k0 + 3]) * inv0);
     uint32_t lo1 = cvt_e4m3x2(bf16_hi(w[k0]) * inv1, bf16_hi(w[k0 + 1]) * inv1);
-    uint32_t hi1 = cvt_e4m3x2(bf16_hi(w[k0 + 8]) * inv1, bf16_hi(w[k0 + 9]) * inv1);
+    uint32_t hi1 = cvt_e4m3x2(bf16_hi(w[k0 + 2]) * inv1, bf16_hi(w[k0 + 3]) * inv1);
     o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu : (lo0 | (hi0 << 16));
     o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
   }
   const int d0 = 2 * dp, d1 = 2 * dp + 1;
-  const bool valid = s0 + kb * 32 < S;   // whole 32-token blocks
-  if (valid) {
+  if (s0 + kb * 32 < S) {   // whole 32-token blocks
     uint8_t* row0 = vt + ((long long)plane * 128 + d0) * S + s0 + kb * 32;
     uint8_t* row1 = vt + ((long long)plane * 128 + d1) * S + s0 + kb * 32;
     __stcs(reinterpret_cast<uint4*>(row0), make_uint4(o0[0], o0[1], o0[2], o0[3]));
     __stcs(reinterpret_cast<uint4*>(row0) + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
     __stcs(reinterpret_cast<uint4*>(row1), make_uint4(o1[0], o1[1], o1[2], o1[3]));
     __stcs(reinterpret_cast<uint4*>(row1) + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
+    const long long blk_idx = (long long)plane * (S / 32) + s0 / 32 + kb;
+    *reinterpret_cast<uint16_t*>(vsc + blk_idx * 128 + d0) = (uint16_t)(sb0 | (sb1 << 8));
   }
-  uint8_t* atom = vsc + ((long long)plane * ntiles + tile_idx) * 512;
-  atom[atom_word_offset(d0) + kb] = valid ? (uint8_t)sb0 : (uint8_t)0;
-  atom[atom_word_offset(d1) + kb] = valid ? (uint8_t)sb1 : (uint8_t)0;
 }
 
 __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
@@ -239,7 +216,6 @@ cudaError_t launch_quant_rowwise(const void* x, uint8_t* q, uint8_t* sc, int B, 
   const long long grid = (long long)B * H * ((S + RW_ROWS - 1) / RW_ROWS);
   quant_rowwise_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(x), q, sc, B, S, H, layout,
                                                         rule);
-  if (S % 128 != 0) pad_row_atoms_kernel<<<(unsigned)((long long)B * H), 128, 0, st>>>(sc, S);
   return cudaGetLastError();
 }
 
@@ -249,10 +225,6 @@ cudaError_t launch_quant_qkv(QkvQuantArgs a, cudaStream_t st) {
   a.nq_blocks = (long long)a.B * a.Hq * nchunk;
   const long long nk_blocks = (long long)a.B * a.Hkv * nchunk;
   quant_qkv_kernel<<<(unsigned)(a.nv_blocks + a.nq_blocks + nk_blocks), 256, 0, st>>>(a);
-  if (a.S % 128 != 0) {
-    pad_row_atoms_kernel<<<(unsigned)((long long)a.B * a.Hq), 128, 0, st>>>(a.q_sc, a.S);
-    pad_row_atoms_kernel<<<(unsigned)((long long)a.B * a.Hkv), 128, 0, st>>>(a.k_sc, a.S);
-  }
   return cudaGetLastError();
 }
 

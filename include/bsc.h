@@ -15,34 +15,27 @@
  *     synchronises; all work is enqueued on `stream` (NULL = the legacy default stream).
  *   - Arguments are checked before anything is enqueued; on any error nothing is launched.
  *   - Calls hold no state between invocations and may be made from several host threads.
- *   - Tokens S must be a multiple of 32 (whole MX blocks) and D must be 128.  Work is tiled by 128
- *     tokens; T = ceil(S/128) is the number of tiles per (b, h), the last one possibly partial.
- *     B, S or H equal to 0 is an empty
- *     problem: the call returns BSC_OK and launches nothing (pointers are not inspected).
+ *   - Tokens S must be a multiple of 32 (whole MX blocks) and D must be 128.  B, S or H equal to 0
+ *     is an empty problem: the call returns BSC_OK and launches nothing (pointers are not
+ *     inspected).
  *   - Every pointer must be 16-byte aligned.
  *   - The current CUDA device must be compute capability 10.3 (GB300).
  *   - Inputs are assumed finite; a NaN/Inf V value in a later token can reach earlier rows
  *     through a 0 * NaN product inside the diagonal key tile.
  *
- * Data layouts (BSHD: [B][S][H][D]; SBHD: [S][B][H][D]; D fastest in both):
+ * Data layouts (BSHD: [B][S][H][D]; SBHD: [S][B][H][D]; D fastest in both).  Every scale array is
+ * compact, in the operation's natural order (no padding, no swizzle):
  *   x_bf16, v_bf16, o_bf16    bf16 in the given layout
  *   x_e4m3, vtn_e4m3          E4M3 bytes, same layout and strides as the bf16 input
- *   v_e4m3_t                  E4M3 bytes of V transposed, [B][H][D][S], with the tokens of each
- *                             aligned 32-token block in the order the attention kernel's P operand
- *                             uses: byte 32*blk + x holds token 32*blk + perm32(x), where
- *                             perm32(x) = 8*((x%8)/2) + 2*(x/8) + x%2 (a 4x4 transpose of token
- *                             pairs; perm32(perm32(x)) = x).  Scales are unaffected: a block keeps
- *                             its 32 tokens.
- *   Scale bytes are E8M0 (value 2^(byte-127); 0xFF = NaN) and come in two forms:
- *   "row atoms" (Q and K rowwise scales):  one byte per (b, h, s, c) with c = d/32, at
- *        ((b*H + h)*T + s/128)*512 + (s%32)*16 + ((s%128)/32)*4 + c
- *   "column atoms" (V columnwise scales): one byte per (b, h, d, 32-token block), at
- *        ((b*H + h)*T + s/128)*512 + (d%32)*16 + (d/32)*4 + (s%128)/32
- *     Both are the 128x4 scale-factor atom order read by the tensor cores (each 512-byte atom
- *     covers 128 rows x 4 blocks of 32), so the attention kernel copies atoms unchanged.  Both take
- *     B*H*T*512 bytes; in the last atom of a partial tile the bytes of tokens past S are written 0.
- *   vtn_sc                    token amplitudes, one byte per (b, h, s) at (b*H + h)*S + s
+ *   v_e4m3_t                  E4M3 bytes of V transposed, [B][H][D][S] (tokens in order)
+ *   x_sc (Q, K and MXFP8 O)   one scale byte per (b, h, s, 32-element block c = d/32):
+ *                             [B][H][S][D/32], byte ((b*H + h)*S + s)*4 + c
+ *   v_sc                      one scale byte per (b, h, 32-token block, d):
+ *                             [B][H][S/32][D], byte ((b*H + h)*(S/32) + s/32)*D + d
+ *   vtn_sc                    one token amplitude per (b, h, s): [B][H][S], byte (b*H + h)*S + s
  *   lse                       fp32 [B][Hq][S], natural log
+ * Scale bytes are E8M0: value 2^(byte-127), 0xFF = NaN.  The attention kernels permute scales
+ * into the tensor cores' scale-factor order themselves.
  *
  * Quantisation rule (OCP MX, E4M3 elements): for a block with maximum magnitude amax, the scale
  * byte is clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for amax = 0); each element is x*2^-e
@@ -83,8 +76,7 @@ const char* bsc_status_string(bsc_status s);
 /*
  * Rowwise MXFP8 quantisation of Q or K: one E8M0 scale per 32 consecutive elements along D of
  * each (b, s, h) row ("Q/K decoded from their rowwise MXFP8 bytes", PR #3865 Description).
- *   x_bf16 [in]  bf16 in `layout`;  x_e4m3 [out] same layout;  x_sc [out] row atoms,
- *   B*H*T*512 bytes.
+ *   x_bf16 [in]  bf16 in `layout`;  x_e4m3 [out] same layout;  x_sc [out] [B][H][S][D/32].
  */
 bsc_status mxfp8_quantize_qk_rowwise(const void* x_bf16, int B, int S, int H, int D, bsc_layout layout,
                                      uint8_t* x_e4m3, uint8_t* x_sc, bsc_stream_t stream);
@@ -92,9 +84,7 @@ bsc_status mxfp8_quantize_qk_rowwise(const void* x_bf16, int B, int S, int H, in
 /*
  * Columnwise MXFP8 quantisation of V: one E8M0 scale per 32 consecutive tokens of each (b, h, d)
  * ("A columnwise MXFP8 V scale is shared by 32 consecutive tokens", PR #3865 Description).
- *   v_bf16 [in] bf16 in `layout`;  v_e4m3_t [out] [B][H][D][S] (perm32 order within 32-token
- *   blocks);  v_sc [out] column atoms,
- *   B*H*T*512 bytes.
+ *   v_bf16 [in] bf16 in `layout`;  v_e4m3_t [out] [B][H][D][S];  v_sc [out] [B][H][S/32][D].
  */
 bsc_status mxfp8_quantize_v_colwise(const void* v_bf16, int B, int S, int H, int D, bsc_layout layout,
                                     uint8_t* v_e4m3_t, uint8_t* v_sc, bsc_stream_t stream);
@@ -135,7 +125,7 @@ typedef struct {
   int layout;             /* bsc_layout */
   int rule;               /* bsc_scale_rule */
   uint8_t* e4m3;          /* [out] rowwise bytes, or V columnwise bytes [B][H][D][S] */
-  uint8_t* sc;            /* [out] row atoms (rowwise) or column atoms (V columnwise) */
+  uint8_t* sc;            /* [out] [B][H][S][D/32] (rowwise) or [B][H][S/32][D] (V columnwise) */
   uint8_t* vtn_e4m3;      /* [out] token-normalised V bytes (token-norm and fused kinds) */
   uint8_t* vtn_sc;        /* [out] token amplitudes (token-norm and fused kinds) */
 } bsc_quant_params;
@@ -177,22 +167,23 @@ bsc_status mxfp8_quantize_qkv(const bsc_qkv_quant_params* p, bsc_stream_t stream
 
 typedef struct {
   const uint8_t* q;       /* [in] Q E4M3 bytes, `layout`, Hq heads */
-  const uint8_t* q_sc;    /* [in] Q row atoms */
+  const uint8_t* q_sc;    /* [in] Q scales [B][Hq][S][D/32] */
   const uint8_t* k;       /* [in] K E4M3 bytes, `layout`, Hkv heads */
-  const uint8_t* k_sc;    /* [in] K row atoms */
-  const uint8_t* v_t;     /* [in] V columnwise E4M3 bytes, [B][Hkv][D][S], perm32 order */
-  const uint8_t* v_sc;    /* [in] V column atoms */
+  const uint8_t* k_sc;    /* [in] K scales [B][Hkv][S][D/32] */
+  const uint8_t* v_t;     /* [in] V columnwise E4M3 bytes, [B][Hkv][D][S] */
+  const uint8_t* v_sc;    /* [in] V columnwise scales [B][Hkv][S/32][D] */
   const uint8_t* vtn;     /* [in] token-normalised V bytes, `layout` (unused when leaky = 1) */
   const uint8_t* vtn_sc;  /* [in] token amplitudes [B][Hkv][S] (unused when leaky = 1) */
   void* o;                /* [out] bf16 O in `layout`, Hq heads (may be NULL when o_e4m3 is set) */
   float* lse;             /* [out] [B][Hq][S], ln sum_{j<=i} exp(softmax_scale * q_i . k_j) */
   int B, S, Hq, Hkv, D;
   int layout;             /* bsc_layout */
-  float softmax_scale;
-  /* Number of E4M3 terms P is split into for the MXFP8 P.V of completed blocks (1 or 2).  P is
-   * quantised after the running-max subtraction with a constant scale (2^-8; the second term
-   * carries the residual at 2^-12), so the scale never depends on data.  The own block uses the
-   * same number of BF16 terms. */
+  float softmax_scale;    /* finite and > 0, else BSC_ERR_UNSUPPORTED */
+  /* Number of E4M3 terms P is split into for the MXFP8 P.V of completed blocks (1 or 2).  Each
+   * row's weights are quantised per 32-key block with a power-of-two scale chosen from that row's
+   * own scores in that block (the block's largest weight lands in [128, 256)), so a scale never
+   * depends on another row or on a key the row cannot see.  The second term is the E4M3 residual
+   * at the same scale.  The own block is one BF16 term. */
   int p_terms;
   /* 0: the method.  1: ordinary (leaky) causal MXFP8 - the own block is attended with the
    * columnwise V as well; a control that shows the leak. */
@@ -207,11 +198,10 @@ typedef struct {
   int debug_stall;
   /* Optional MXFP8 O ("FROST SDPA fp8: block-scaled O epilogues (NVFP4 / MXFP8) with an sf_o
    * output", cudnn-frontend PR #1088 and its follow-up #1180, Summary: FP8_E4M3 O with one UE8M0
-   * scale per 32 head-dim elements, scales in the F8_128x4 atom order as per-(b, h) planes).
-   * When o_e4m3 is not NULL the epilogue also writes O as E4M3 bytes in `layout` (Hq heads) and
-   * o_sc as row atoms exactly like Q's scales (B*Hq*T*512 bytes, bytes past S written 0), by the
-   * quantisation rule above applied to the fp32 O before any BF16 rounding.  o_sc is required
-   * with o_e4m3. */
+   * scale per 32 head-dim elements; that page keeps the scales in its swizzled atom order, this
+   * library in the compact order of Q's scales).  When o_e4m3 is not NULL the epilogue also writes O as E4M3 bytes in `layout` (Hq heads) and
+   * o_sc [B][Hq][S][D/32] like Q's scales, by the quantisation rule above applied to the fp32 O
+   * before any BF16 rounding.  o_sc is required with o_e4m3. */
   uint8_t* o_e4m3;
   uint8_t* o_sc;
 } bsc_attn_fwd_params;
@@ -225,9 +215,9 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
 
 typedef struct {
   const uint8_t* q;       /* [in] Q E4M3 bytes, `layout`, Hq heads */
-  const uint8_t* q_sc;    /* [in] Q row atoms */
+  const uint8_t* q_sc;    /* [in] Q scales [B][Hq][S][D/32] */
   const uint8_t* k;       /* [in] K E4M3 bytes, `layout`, Hkv heads */
-  const uint8_t* k_sc;    /* [in] K row atoms */
+  const uint8_t* k_sc;    /* [in] K scales [B][Hkv][S][D/32] */
   const uint8_t* vtn;     /* [in] token-normalised V bytes, `layout`, Hkv heads */
   const uint8_t* vtn_sc;  /* [in] token amplitudes [B][Hkv][S] */
   const void* o;          /* [in] bf16 O of the forward, `layout`, Hq heads */
@@ -238,7 +228,7 @@ typedef struct {
   void* dv;               /* [out] bf16, `layout`, Hkv heads */
   int B, S, Hq, Hkv, D;
   int layout;             /* bsc_layout */
-  float softmax_scale;
+  float softmax_scale;    /* finite and > 0, else BSC_ERR_UNSUPPORTED */
   int32_t* dev_status;    /* optional, as in bsc_attn_fwd_params */
   uint32_t wait_timeout_ms;
 } bsc_attn_bwd_params;

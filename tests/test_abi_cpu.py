@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(ops):
 def test_status_strings(ops):
     for code in range(7):
         assert ops.lib.bsc_status_string(code).decode().startswith("BSC_")
-    assert ops.lib.bsc_abi_version() == 2
+    assert ops.lib.bsc_abi_version() == 3
 
 
 def test_params_struct_layout(ops):
@@ -89,6 +89,10 @@ def _params(ops, **kw):
     (dict(S=200), 4),
     (dict(p_terms=3), 4),
     (dict(leaky=2), 4),
+    (dict(softmax_scale=0.0), 4),                 # the scale must be finite and positive
+    (dict(softmax_scale=-0.088), 4),
+    (dict(softmax_scale=float("nan")), 4),
+    (dict(softmax_scale=float("inf")), 4),
     (dict(layout=2), 2),
     (dict(o=0), 1),
     (dict(vtn=0), 1),
@@ -100,6 +104,17 @@ def _params(ops, **kw):
 def test_attn_validation(ops, kw, want):
     p = _params(ops, **kw)
     assert ops.lib.mxfp8_causal_attn_fwd(ctypes.byref(p), None) == want
+
+
+def test_bwd_validation(ops):
+    base = dict(q=FAKE, q_sc=FAKE, k=FAKE, k_sc=FAKE, vtn=FAKE, vtn_sc=FAKE, o=FAKE, lse=FAKE, d_o=FAKE, dq=FAKE,
+                dk=FAKE, dv=FAKE, B=1, S=256, Hq=4, Hkv=2, D=128, layout=0, softmax_scale=0.088, dev_status=0,
+                wait_timeout_ms=0)
+    for kw, want in ((dict(softmax_scale=-1.0), 4), (dict(softmax_scale=float("nan")), 4), (dict(Hq=3), 2),
+                     (dict(dq=0), 1), (dict(dk=FAKE + 8), 3), (dict(S=0), 0)):
+        p = ops.AttnBwdParams(**dict(base, **kw))
+        assert ops.lib.bf16_attn_bwd(ctypes.byref(p), None) == want, kw
+    assert ops.lib.bf16_attn_bwd(None, None) == 1
 
 
 def test_attn_null_params(ops):
@@ -165,12 +180,3 @@ def test_qkv_quant_validation(ops, kw, want):
     p = ops.QkvQuantParams(**base)
     assert ops.lib.mxfp8_quantize_qkv(ctypes.byref(p), None) == want
 
-
-def test_perm32_is_an_involution_within_blocks():
-    import numpy as np
-    from tests._helpers import perm32, vt_to_token_order
-    p = perm32()
-    assert sorted(p) == list(range(32)) and (p[p] == np.arange(32)).all()
-    x = np.arange(64, dtype=np.int64)[None]
-    y = vt_to_token_order(x)
-    assert (y[0, :32] == p).all() and (y[0, 32:] == 32 + p).all()

@@ -7,7 +7,7 @@ import torch
 
 from block_scaled_causal_gb300 import inputs as I
 from oracle import mx
-from tests._helpers import bshd_np, col_atoms_to_compact, row_atoms_to_compact, vt_to_token_order
+from tests._helpers import bshd_np, vsc_as_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +23,7 @@ def _check_rowwise(ops, x_cpu, layout, rows=None):
     torch.cuda.synchronize()
     xb = bshd_np(x_cpu, layout).astype(np.float64)
     gq = bshd_np(xq, layout)
-    gs = row_atoms_to_compact(xsc.cpu().numpy())
+    gs = xsc.cpu().numpy()
     if rows is not None:                   # the rule is per row: a subset of tokens is the same check
         xb, gq, gs = xb[:, rows], gq[:, rows], gs[:, :, rows]
     oq, os_ = mx.quantize_rowwise(xb)
@@ -39,8 +39,8 @@ def _check_v(ops, v_cpu, layout, tokens=None):
     for a, b in ((vt, vt2), (vsc, vsc2), (vtn, vtn2), (vtn_sc, vtn_sc2)):
         assert torch.equal(a, b)
     vb = bshd_np(v_cpu, layout).astype(np.float64)
-    g_vt = vt_to_token_order(vt.cpu().numpy())
-    g_vsc = col_atoms_to_compact(vsc.cpu().numpy())
+    g_vt = vt.cpu().numpy()
+    g_vsc = vsc_as_oracle(vsc.cpu().numpy())
     g_vtn = bshd_np(vtn, layout)
     g_vtn_sc = vtn_sc.cpu().numpy()
     if tokens is not None:                 # whole 128-token tiles
@@ -126,7 +126,7 @@ def test_guard_bands_untouched(ops):
     buf = torch.full((n + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda")
     sbuf = torch.full((B * H * S * 4 + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
     out = buf[pad:pad + n].view(B, S, H, 128)
-    osc = sbuf[pad:pad + B * H * S * 4].view(B, H, S // 128, 512)
+    osc = sbuf[pad:pad + B * H * S * 4].view(B, H, S, 4)
     ops.mxfp8_quantize_qk_rowwise(x, I.BSHD, out=out, out_sc=osc)
     torch.cuda.synchronize()
     assert bool((buf[:pad] == 0xA5).all()) and bool((buf[pad + n:] == 0xA5).all())

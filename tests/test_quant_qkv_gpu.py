@@ -12,7 +12,7 @@ import torch
 
 from block_scaled_causal_gb300 import inputs as I
 from oracle import mx
-from tests._helpers import bshd_np, col_atoms_to_compact, row_atoms_to_compact, vt_to_token_order
+from tests._helpers import bshd_np, vsc_as_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -52,16 +52,12 @@ def test_qkv_against_oracle(ops):
     S = w.S
     for x, xq, xs in ((q, qq, qs), (k, kq, ks)):
         oc, osc = mx.quantize_rowwise(bshd_np(x, w.layout).astype(np.float64))
-        gs = row_atoms_to_compact(xs.cpu().numpy())
-        np.testing.assert_array_equal(gs[:, :, :S], osc)
-        assert not gs[:, :, S:].any()
+        np.testing.assert_array_equal(xs.cpu().numpy(), osc)
         np.testing.assert_array_equal(bshd_np(xq, w.layout), oc)
     vb = bshd_np(v, w.layout).astype(np.float64)
     cc, ccs = mx.quantize_colwise(vb)
-    g_vsc = col_atoms_to_compact(vsc.cpu().numpy())
-    np.testing.assert_array_equal(g_vsc[..., : S // 32], ccs)
-    assert not g_vsc[..., S // 32:].any()
-    np.testing.assert_array_equal(vt_to_token_order(vt.cpu().numpy()), cc)
+    np.testing.assert_array_equal(vsc_as_oracle(vsc.cpu().numpy()), ccs)
+    np.testing.assert_array_equal(vt.cpu().numpy(), cc)
     tn, tns = mx.quantize_token_norm(vb)
     np.testing.assert_array_equal(vtn_sc.cpu().numpy(), tns)
     np.testing.assert_array_equal(bshd_np(vtn, w.layout), tn)
