@@ -60,23 +60,33 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that suspends the thread until the phase completes or about `ns` nanoseconds pass,
+// instead of returning at once: a waiting thread then issues no further shared-memory traffic.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p;}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with `parity` of an mbarrier, fully inline (a call would make the
 // caller save its live registers).  An inline non-blocking test first (the common case, where the
-// phase completed already), then try_wait in a loop bounded by the wall clock.  Returns false if
+// phase completed already), then suspending try_waits bounded by the wall clock.  Returns false if
 // another thread of the CTA has aborted, or if this wait ran past the limit (then it records
 // `site` in the device status word and raises the CTA's abort flag).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*ctl.abort_flag) return false;
-      if (globaltimer_ns() - t0 > ctl.limit_ns) {
-        *ctl.abort_flag = 1;
-        if (ctl.dev_status) atomicCAS(ctl.dev_status, 0, 0x100 | site);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*ctl.abort_flag) return false;
+    if (globaltimer_ns() - t0 > ctl.limit_ns) {
+      *ctl.abort_flag = 1;
+      if (ctl.dev_status) atomicCAS(ctl.dev_status, 0, 0x100 | site);
+      return false;
     }
   }
 }
@@ -84,7 +94,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // Wait that ignores the abort flag (for draining copies this thread issued itself), still bounded.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
