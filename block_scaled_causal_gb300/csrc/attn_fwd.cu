@@ -528,9 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // 2^(s - m) over the keys so far.
     float m = -INFINITY, l = 0.f;
     bool ok = start_ok;
-    for (int j = 0; j <= t; ++j) {
+    // One key tile.  The diagonal tile (DIAG) has its own instantiation, peeled out of the loop, so
+    // that the loop body holds only the code of ordinary tiles.
+    auto tile = [&](int j, auto diag_tag) {
+      constexpr bool DIAG = decltype(diag_tag)::value;
       const int sb = j & 1;
-      const bool diag = j == t;
       // one pass of work; a failed wait leaves it early (break), the tile's barrier generation is
       // still met below
       do {
@@ -541,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
       for (int c = 0; c < 4; ++c) tld32(tmem + lane_off + (sb ? T_S1 : T_S0) + 32 * c, v + 32 * c);
       tmem_ld_wait();
-      if (diag) {   // keys after the row (key index = column inside the diagonal tile)
+      if constexpr (DIAG) {   // keys after the row (key index = column inside the diagonal tile)
 #pragma unroll
         for (int k = 0; k < 128; ++k) v[k] = k > r ? -INFINITY : v[k];
       }
@@ -590,13 +592,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       m = m_new;
       uint32_t w0[32], w1[32], own[16];
       uint32_t sfw;
-      if (OWN && diag) sfw = block_p<P_TERMS, true>(v, bm, m, sl2, q, w0, w1, own, l);
+      if constexpr (OWN && DIAG) sfw = block_p<P_TERMS, true>(v, bm, m, sl2, q, w0, w1, own, l);
       else sfw = block_p<P_TERMS, false>(v, bm, m, sl2, q, w0, w1, own, l);
       // P over this tile's S buffer (its scores are in registers); the S_FULL completion above
       // implies that the P.V two tiles back, the last reader of the buffer and of this parity's
       // scale columns, has completed
       const uint32_t tP = tmem + lane_off + (sb ? T_S1 : T_S0);
-      if (OWN && diag) {
+      if constexpr (OWN && DIAG) {
         tst16(tP, w0);
         tst8(tP + 16, w0 + 16);
         if (P_TERMS > 1) {
@@ -635,7 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       } else {
         named_sync(NB_P + sb, kNbP);
       }
-    }
+    };
+    for (int j = 0; j < t; ++j) tile(j, std::false_type{});
+    tile(t, std::true_type{});
     // ---- epilogue: O / l -> BF16 (and/or MXFP8), LSE
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_O_FULL), 0, ctl, W_SM_O));
     if (ok) {
