@@ -199,7 +199,8 @@ typedef struct {
   /* Optional MXFP8 O ("FROST SDPA fp8: block-scaled O epilogues (NVFP4 / MXFP8) with an sf_o
    * output", cudnn-frontend PR #1088 and its follow-up #1180, Summary: FP8_E4M3 O with one UE8M0
    * scale per 32 head-dim elements; that page keeps the scales in its swizzled atom order, this
-   * library in the compact order of Q's scales).  When o_e4m3 is not NULL the epilogue also writes O as E4M3 bytes in `layout` (Hq heads) and
+   * library in the compact order of Q's scales).  When o_e4m3 is not NULL the epilogue also
+   * writes O as E4M3 bytes in `layout` (Hq heads) and
    * o_sc [B][Hq][S][D/32] like Q's scales, by the quantisation rule above applied to the fp32 O
    * before any BF16 rounding.  o_sc is required with o_e4m3. */
   uint8_t* o_e4m3;
@@ -210,6 +211,11 @@ typedef struct {
  * Leak-free causal MXFP8 attention forward (PR #3865 Description: completed-block MXFP8 part,
  * own-block part on the token-normalised V, log-sum-exp merge).  GQA: query head h reads
  * KV head h / (Hq/Hkv).  Returns BF16 O and/or MXFP8 O, and fp32 LSE.
+ * Causality: for finite inputs, row i of every output is bit-for-bit independent of the tokens
+ * after i.  V must be finite for that to hold inside a 128-token tile: the diagonal tile's MMAs
+ * multiply the zero weights of a row's later keys with those keys' V, and 0 x NaN (or 0 x the NaN
+ * that a non-finite V block encodes to) is NaN, so a non-finite V element of token j makes the
+ * earlier rows of j's 128-token tile non-finite.  Rows of earlier tiles never read token j.
  */
 bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stream);
 

@@ -184,3 +184,43 @@ def causal_attention_bwd(qh, kh, vt, o, lse, do, scale, chunk=256):
                 dq[b, ri, hq, :] += scale * (ds @ kh[b, :kmax, hk, :])
                 dk[b, :kmax, hk, :] += scale * (ds.T @ qh[b, ri, hq, :])
     return dq, dk, dv
+
+
+def causal_attention_bwd_sampled(qh, kh, vt, o, lse, do, scale, rows, keys):
+    """causal_attention_bwd restricted to dQ at the query `rows` and dK, dV at the key positions
+    `keys`, by the same formulas (PR #3865 page, Description, Backward).  dQ_i reads row i's O and
+    LSE; dK_j and dV_j sum over every row i >= j and read those rows' O and LSE, so only they need
+    to be meaningful in `o` and `lse`.
+
+    qh, do, o [B,S,Hq,D]; kh, vt [B,S,Hkv,D]; lse [B,Hq,S].  Returns dq [B,len(rows),Hq,D] and
+    dk, dv [B,len(keys),Hkv,D].
+    """
+    qh, kh, vt, o, lse, do = (np.asarray(a, dtype=np.float64) for a in (qh, kh, vt, o, lse, do))
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.asarray(keys, dtype=np.int64)
+    B, S, Hq, D = qh.shape
+    Hkv = kh.shape[2]
+    g = Hq // Hkv
+    dq = np.zeros((B, len(rows), Hq, D))
+    dk = np.zeros((B, len(keys), Hkv, D))
+    dv = np.zeros((B, len(keys), Hkv, D))
+    for b in range(B):
+        for hq in range(Hq):
+            hk = hq // g
+            for n, i in enumerate(rows):
+                s = scale * (kh[b, : i + 1, hk, :] @ qh[b, i, hq, :])                 # keys j <= i
+                p = np.exp(s - lse[b, hq, i])
+                dp = vt[b, : i + 1, hk, :] @ do[b, i, hq, :]
+                ds = p * (dp - np.dot(do[b, i, hq, :], o[b, i, hq, :]))
+                dq[b, n, hq, :] = scale * (ds @ kh[b, : i + 1, hk, :])
+            if len(keys) == 0:
+                continue
+            ri = np.arange(int(keys.min()), S)                                      # rows i >= min key
+            s = scale * (qh[b, ri, hq, :] @ kh[b, keys, hk, :].T)                   # [R, K]
+            visible = keys[None, :] <= ri[:, None]
+            p = np.where(visible, np.exp(np.where(visible, s, 0.0) - lse[b, hq, ri][:, None]), 0.0)
+            dp = do[b, ri, hq, :] @ vt[b, keys, hk, :].T
+            ds = p * (dp - np.sum(do[b, ri, hq, :] * o[b, ri, hq, :], axis=1)[:, None])
+            dv[b, :, hk, :] += p.T @ do[b, ri, hq, :]
+            dk[b, :, hk, :] += scale * (ds.T @ qh[b, ri, hq, :])
+    return dq, dk, dv

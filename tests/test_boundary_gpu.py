@@ -106,3 +106,34 @@ def test_bounded_wait_reports_timeout_and_context_survives(ops):
     o, lse = ops.mxfp8_causal_attn_fwd(*args, layout=w.layout, softmax_scale=w.scale, dev_status=status)
     assert ops.bsc_read_device_status(status) == ops.BSC_OK
     assert torch.isfinite(o.float()).all()
+
+
+@pytest.mark.parametrize("layout,B,S", [(I.BSHD, 1, 416), (I.SBHD, 2, 160)])
+def test_attention_on_oracle_quantised_compact_operands(ops, layout, B, S):
+    """The C ABI's operand layouts as documented: E4M3 bytes in the input's layout, compact rowwise
+    scales [B,H,S,D/32], V bytes transposed to [B,H,D,S] in natural token order with scales
+    [B,H,S/32,D], token-normalised bytes in the input's layout with amplitudes [B,H,S].  Operands
+    built by the oracle's quantisers (not the library's) give bit-for-bit the output of the whole
+    path on the bf16 inputs, and match the oracle's attention within the tolerances."""
+    from oracle import attention as A
+    from oracle import mx
+    from tests._helpers import bshd_np
+    from tests.test_attn_gpu import _compare
+    w = I.Workload("x", B, S, 4, 2, layout=layout, v_pattern="every7x16")
+    q, k, v = I.make_qkv(w, seed_offset=90)
+    qb, kb, vb = (bshd_np(t, layout).astype(np.float64) for t in (q, k, v))
+    q8, qsc = mx.quantize_rowwise(qb)
+    k8, ksc = mx.quantize_rowwise(kb)
+    vt, vsc = mx.quantize_colwise(vb)                       # [B,H,D,S], [B,H,D,S/32]
+    vtn, vtn_sc = mx.quantize_token_norm(vb)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    lay = lambda a: I.to_layout(torch.from_numpy(np.ascontiguousarray(a)), layout).cuda()
+    ops_in = (lay(q8), dev(qsc), lay(k8), dev(ksc), dev(vt), dev(np.swapaxes(vsc, -1, -2)), lay(vtn), dev(vtn_sc))
+    o, lse = ops.mxfp8_causal_attn_fwd(*ops_in, layout, w.scale, p_terms=2)
+    o_ref, lse_ref = ops.forward(q.cuda(), k.cuda(), v.cuda(), layout, w.scale, p_terms=2)
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
+    O, L = A.causal_attention(mx.dequantize_rowwise(q8, qsc), mx.dequantize_rowwise(k8, ksc),
+                              mx.dequantize_colwise(vt, vsc), mx.dequantize_token_norm(vtn, vtn_sc), w.scale)
+    print(_compare(bshd_np(o, layout).astype(np.float64), lse.cpu().numpy().astype(np.float64), O, L))

@@ -98,3 +98,81 @@ def test_bwd_dq_causal_bit_exact(ops):
         pert = ops.forward_backward(q2.cuda(), k2.cuda(), v2.cuda(), do2.cuda(), w.layout, w.scale)
         torch.cuda.synchronize()
         assert torch.equal(base[2][:, : i + 1].view(torch.int16), pert[2][:, : i + 1].view(torch.int16)), i
+
+
+def _abs_terms_sampled(qh, kh, vt, o, lse, do, scale, rows, keys):
+    """The tolerance terms of _abs_terms at the sampled dQ rows and dK, dV keys."""
+    B, S, Hq, D = qh.shape
+    g = Hq // kh.shape[2]
+    tq = np.zeros((B, len(rows), Hq, D))
+    tk = np.zeros((B, len(keys), kh.shape[2], D))
+    tv = np.zeros_like(tk)
+    for b in range(B):
+        for hq in range(Hq):
+            hk = hq // g
+            for n, i in enumerate(rows):
+                p = np.exp(scale * (kh[b, : i + 1, hk] @ qh[b, i, hq]) - lse[b, hq, i])
+                ds = np.abs(p * (vt[b, : i + 1, hk] @ do[b, i, hq] - np.dot(do[b, i, hq], o[b, i, hq])))
+                tq[b, n, hq] = scale * ds @ np.abs(kh[b, : i + 1, hk])
+            ri = np.arange(int(keys.min()), S)
+            vis = keys[None, :] <= ri[:, None]
+            p = np.where(vis, np.exp(np.where(vis, scale * qh[b, ri, hq] @ kh[b, keys, hk].T, 0.0)
+                                     - lse[b, hq, ri][:, None]), 0.0)
+            ds = np.abs(p * (do[b, ri, hq] @ vt[b, keys, hk].T - np.sum(do[b, ri, hq] * o[b, ri, hq], axis=1)[:, None]))
+            tv[b, :, hk] += p.T @ np.abs(do[b, ri, hq])
+            tk[b, :, hk] += scale * ds.T @ np.abs(qh[b, ri, hq])
+    return tq, tk, tv
+
+
+def test_bwd_b2_s32k_sbhd_sampled(ops):
+    """B=2, Hq=Hkv=16, S=32768, SBHD (the shape the pages time forward + backward on): dQ at sampled
+    rows and dK, dV at sampled keys among the last 512 tokens, query heads 0 and 15, against the
+    oracle's sampled backward.  O and LSE of every row those outputs read (the sampled rows and all
+    rows from the first sampled key on) come from the oracle's forward, rounded to the BF16 and fp32
+    the call takes, and both sides get them; the other rows keep the library forward's values,
+    which no checked output reads."""
+    w = I.WORKLOADS["mha_b2_s32k_h16_sbhd"]
+    S, L = w.S, w.layout
+    q, k, v, do = I.make_qkv(w, with_do=True)
+    heads = [0, 15]
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 31, 32, 4095, 4096, S - 600, S - 1], rng.integers(0, S, 6)]))
+    keys = np.unique(np.concatenate([[S - 512, S - 481, S - 480, S - 129, S - 128, S - 33, S - 32, S - 1],
+                                     rng.integers(S - 512, S, 4)]))
+    need = np.union1d(rows, np.arange(int(keys.min()), S))
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    qq, qs, kq, ks, vt, vsc, vtn, vtn_sc = ops.mxfp8_quantize_qkv(qd, kd, vd, L)
+    o, lse = ops.mxfp8_causal_attn_fwd(qq, qs, kq, ks, vt, vsc, vtn, vtn_sc, L, w.scale, p_terms=2)
+    # the oracle's operands for the two heads (quantisation is per row / token / head, so the
+    # head slice quantises exactly as the whole tensor does)
+    f64 = lambda t: bshd_np(t[:, :, heads], L).astype(np.float64)
+    qb, kb, vb, dob = f64(q), f64(k), f64(v), f64(do)
+    qh = mx.dequantize_rowwise(*mx.quantize_rowwise(qb))
+    kh = mx.dequantize_rowwise(*mx.quantize_rowwise(kb))
+    vc = mx.dequantize_colwise(*mx.quantize_colwise(vb))
+    vtt = mx.dequantize_token_norm(*mx.quantize_token_norm(vb))
+    O_n, L_n = A.causal_attention(qh, kh, vc, vtt, w.scale, rows=need)           # [B,n,2,D], [B,2,n]
+    O_bf = torch.from_numpy(O_n).to(torch.bfloat16)
+    L_f32 = torch.from_numpy(L_n).to(torch.float32)
+    ob = I.to_bshd(o, L)
+    nt = torch.from_numpy(need).cuda()
+    for j, h in enumerate(heads):
+        ob[:, nt, h] = O_bf[:, :, j].cuda()
+        lse[:, h, nt] = L_f32[:, j].cuda()
+    dq, dk, dv = ops.bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o, lse, dod, L, w.scale)
+    torch.cuda.synchronize()
+    O_full = np.zeros(qh.shape)
+    O_full[:, need] = O_bf.float().numpy().astype(np.float64)
+    L_full = np.zeros((w.B, len(heads), S))
+    L_full[:, :, need] = L_f32.numpy().astype(np.float64)
+    rq, rk, rv = A.causal_attention_bwd_sampled(qh, kh, vtt, O_full, L_full, dob, w.scale, rows, keys)
+    tq, tk, tv = _abs_terms_sampled(qh, kh, vtt, O_full, L_full, dob, w.scale, rows, keys)
+    out = []
+    for name, g, sel, r, t in (("dq", dq, rows, rq, tq), ("dk", dk, keys, rk, tk), ("dv", dv, keys, rv, tv)):
+        gg = I.to_bshd(g, L)[:, torch.from_numpy(sel).cuda()][:, :, heads].float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(gg)), name
+        err = np.abs(gg - r)
+        bound = 2.0 ** -7 * t + bf16_half_ulp(r) + 1e-6
+        assert np.all(err <= bound), "%s: worst excess %.3e (max err %.3e)" % (name, (err - bound).max(), err.max())
+        out.append("%s max %.2e" % (name, err.max()))
+    print(", ".join(out))

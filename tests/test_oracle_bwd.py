@@ -82,3 +82,30 @@ def test_bwd_causality():
     _, dk3, dv3 = A.causal_attention_bwd(q3, k, v, O3, L3, do3, scale)
     np.testing.assert_allclose(dk[:, i:], dk3[:, i:], rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(dv[:, i:], dv3[:, i:], rtol=1e-13, atol=1e-13)
+
+
+def test_bwd_sampled_matches_full():
+    """The sampled backward gives the full backward's dQ rows and dK, dV keys (GQA, B=2), including
+    the first and last rows and keys on both sides of a 32-token block edge."""
+    B, S, Hq, Hkv, D, scale = 2, 96, 4, 2, 8, 0.4
+    q, k, v = _rand((B, S, Hq, D), 31), _rand((B, S, Hkv, D), 32), _rand((B, S, Hkv, D), 33)
+    do = _rand((B, S, Hq, D), 34)
+    O, L = A.causal_attention(q, k, v, v, scale)
+    dq, dk, dv = A.causal_attention_bwd(q, k, v, O, L, do, scale)
+    rows, keys = np.array([0, 5, 31, 32, 50, 95]), np.array([0, 31, 32, 64, 90, 95])
+    sq, sk, sv = A.causal_attention_bwd_sampled(q, k, v, O, L, do, scale, rows, keys)
+    np.testing.assert_allclose(sq, dq[:, rows], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sk, dk[:, keys], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sv, dv[:, keys], rtol=1e-12, atol=1e-12)
+    # only the rows the sampled outputs read matter: garbage elsewhere changes nothing
+    keys2 = np.array([64, 90, 95])
+    sq, sk, sv = A.causal_attention_bwd_sampled(q, k, v, O, L, do, scale, rows, keys2)
+    O2, L2 = O.copy(), L.copy()
+    other = np.setdiff1d(np.arange(S), np.concatenate([rows, np.arange(keys2.min(), S)]))
+    assert len(other) > 40
+    O2[:, other] = 1e3
+    L2[:, :, other] = -7.0
+    tq, tk, tv = A.causal_attention_bwd_sampled(q, k, v, O2, L2, do, scale, rows, keys2)
+    np.testing.assert_array_equal(tq, sq)
+    np.testing.assert_array_equal(tk, sk)
+    np.testing.assert_array_equal(tv, sv)
