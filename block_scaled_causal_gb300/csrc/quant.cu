@@ -31,16 +31,21 @@ __device__ __forceinline__ uint32_t absmax_bits8(const uint4& v) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Two bf16 values of one word times a power of two (exact), as an fp32 pair (low half first).
+__device__ __forceinline__ float2 scale_bf16x2(uint32_t w, float2 inv2) {
+  return __fmul2_rn(make_float2(bf16_lo(w), bf16_hi(w)), inv2);
+}
+
 // 8 bf16 values (one uint4) * inv_scale -> 8 E4M3 bytes (one uint2).
 __device__ __forceinline__ uint2 quant8(const uint4& v, float inv, bool nonfinite) {
   if (nonfinite) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const float2 inv2 = make_float2(inv, inv);
   uint32_t out[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint16_t p0 = cvt_e4m3x2(bf16_lo(w[2 * i]) * inv, bf16_hi(w[2 * i]) * inv);
-    const uint16_t p1 = cvt_e4m3x2(bf16_lo(w[2 * i + 1]) * inv, bf16_hi(w[2 * i + 1]) * inv);
-    out[i] = (uint32_t)p0 | ((uint32_t)p1 << 16);
+    const float2 a = scale_bf16x2(w[2 * i], inv2), b = scale_bf16x2(w[2 * i + 1], inv2);
+    out[i] = (uint32_t)cvt_e4m3x2(a.x, a.y) | ((uint32_t)cvt_e4m3x2(b.x, b.y) << 16);
   }
   return make_uint2(out[0], out[1]);
 }
@@ -92,7 +97,7 @@ __device__ __forceinline__ void rowwise_rows(const uint8_t* __restrict__ x, uint
   }
 }
 
-__global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
+__global__ void __launch_bounds__(256, 5) quant_rowwise_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
                                                             uint8_t* __restrict__ sc, int B, int S, int H,
                                                             int layout, int rule) {
   rowwise_rows(x, q, sc, B, S, H, layout, rule, blockIdx.x);
@@ -145,29 +150,30 @@ __device__ __forceinline__ void v_tile(const uint8_t* __restrict__ v, uint8_t* _
   if (vt == nullptr) return;
   __syncthreads();
 
-  // columnwise: thread -> (pair of d columns, 32-token block)
+  // columnwise: thread -> (pair of d columns, 32-token block).  Two passes over the staged tile
+  // (the block amax, then the bytes) keep no column in registers.
   const int dp = tid & 63;      // d = 2*dp, 2*dp + 1
   const int kb = tid >> 6;      // 32-token block inside the tile
-  uint32_t w[32];
+  const uint8_t* col = &tile[kb * 32 * VQ_PITCH + dp * 4];
   uint32_t m = 0;
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
-    w[r] = *reinterpret_cast<const uint32_t*>(&tile[(kb * 32 + r) * VQ_PITCH + dp * 4]);
-    uint32_t a = w[r] & 0x7FFF7FFFu;
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(col + r * VQ_PITCH) & 0x7FFF7FFFu;
     asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
   }
   float inv0, inv1;
   const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0, rule);
   const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1, rule);
+  const float2 inv2 = make_float2(inv0, inv1);   // column d0 in the low halves, d1 in the high
   // word i of a column's 32-token block holds tokens 4i..4i+3 (natural order)
   uint32_t o0[8], o1[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int k0 = 4 * i;
-    uint32_t lo0 = cvt_e4m3x2(bf16_lo(w[k0]) * inv0, bf16_lo(w[k0 + 1]) * inv0);
-    uint32_t hi0 = cvt_e4m3x2(bf16_lo(w[k0 + 2]) * inv0, bf16_lo(w[k0 + 3]) * inv0);
-    uint32_t lo1 = cvt_e4m3x2(bf16_hi(w[k0]) * inv1, bf16_hi(w[k0 + 1]) * inv1);
-    uint32_t hi1 = cvt_e4m3x2(bf16_hi(w[k0 + 2]) * inv1, bf16_hi(w[k0 + 3]) * inv1);
+    float2 t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) t[u] = scale_bf16x2(*reinterpret_cast<const uint32_t*>(col + (4 * i + u) * VQ_PITCH), inv2);
+    const uint32_t lo0 = cvt_e4m3x2(t[0].x, t[1].x), hi0 = cvt_e4m3x2(t[2].x, t[3].x);
+    const uint32_t lo1 = cvt_e4m3x2(t[0].y, t[1].y), hi1 = cvt_e4m3x2(t[2].y, t[3].y);
     o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu : (lo0 | (hi0 << 16));
     o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
   }
@@ -184,7 +190,7 @@ __device__ __forceinline__ void v_tile(const uint8_t* __restrict__ v, uint8_t* _
   }
 }
 
-__global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+__global__ void __launch_bounds__(256, 5) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
                                                       uint8_t* __restrict__ vsc, uint8_t* __restrict__ vtn,
                                                       uint8_t* __restrict__ vtn_sc, int B, int S, int H,
                                                       int layout, int rule) {
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint8_t* __restrict_
 // ------------------------------------------------------------------------------------------
 // Q, K and V in one launch: CTAs [0, nv) take V tiles, then Q's 64-token chunks, then K's.  Each
 // CTA does exactly what the matching kernel above does for the same index.
-__global__ void __launch_bounds__(256) quant_qkv_kernel(const __grid_constant__ QkvQuantArgs a) {
+__global__ void __launch_bounds__(256, 5) quant_qkv_kernel(const __grid_constant__ QkvQuantArgs a) {
   __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
   const long long blk = blockIdx.x;
   if (blk < a.nv_blocks) {

@@ -1,7 +1,7 @@
 """GPU backward on decoded operands against the fp64 oracle backward, through the C ABI.
 
 Both sides get the same inputs: the decoded Q, K and token-normalised V (the quantisers are
-bit-exact), the forward's BF16 O and fp32 LSE as the GPU forward returned them, and dO.  The GPU
+bit-exact), O and LSE of the oracle's forward rounded to the BF16 and fp32 the call takes, and dO.  The GPU
 rounds P and dS to BF16 for its MMAs (relative 2^-9) and accumulates in fp32; its outputs are BF16.
 So each element must lie within
     dV: 2^-7 * sum_i P_ij |dO_i|            + half a BF16 ulp
@@ -50,14 +50,22 @@ def _abs_terms(qh, kh, vt, o, lse, do, scale):
 
 def _run_and_check(ops, w, seed):
     q, k, v, do = I.make_qkv(w, seed_offset=seed, with_do=True)
-    o, lse, dq, dk, dv = ops.forward_backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), w.layout, w.scale)
-    torch.cuda.synchronize()
     qb, kb, vb, dob = (bshd_np(t, w.layout).astype(np.float64) for t in (q, k, v, do))
     qh = mx.dequantize_rowwise(*mx.quantize_rowwise(qb))
     kh = mx.dequantize_rowwise(*mx.quantize_rowwise(kb))
+    vc = mx.dequantize_colwise(*mx.quantize_colwise(vb))
     vt = mx.dequantize_token_norm(*mx.quantize_token_norm(vb))
-    og = bshd_np(o, w.layout).astype(np.float64)
-    lg = lse.cpu().numpy().astype(np.float64)
+    # the backward's O and LSE inputs: the oracle forward's, rounded to the BF16 / fp32 the call
+    # takes, given to both sides
+    O, Lo = A.causal_attention(qh, kh, vc, vt, w.scale)
+    o_in = I.to_layout(torch.from_numpy(O).to(torch.bfloat16), w.layout)
+    l_in = torch.from_numpy(Lo).to(torch.float32)
+    og = bshd_np(o_in, w.layout).astype(np.float64)
+    lg = l_in.numpy().astype(np.float64)
+    qq, qs, kq, ks, _, _, vtn, vtn_sc = ops.mxfp8_quantize_qkv(q.cuda(), k.cuda(), v.cuda(), w.layout)
+    dq, dk, dv = ops.bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, o_in.cuda(), l_in.cuda(), do.cuda(), w.layout,
+                                   w.scale)
+    torch.cuda.synchronize()
     rq, rk, rv = A.causal_attention_bwd(qh, kh, vt, og, lg, dob, w.scale)
     tq, tk, tv = _abs_terms(qh, kh, vt, og, lg, dob, w.scale)
     out = []
