@@ -476,7 +476,8 @@ def main():
             refs = {}
             if rank == 0:
                 for hq in heads:
-                    rows_h = np.unique(np.concatenate([sample_rows(wc.S, 11, 7 + hq), [wc.S - 1]]))
+                    # early rows (few keys, so each weight is large) as well as random and last rows
+                    rows_h = np.unique(np.concatenate([[33, 64, 97, 127], sample_rows(wc.S, 8, 7 + hq), [wc.S - 1]]))
                     _, O, L = oracle_sample_step(wc, *cb.cpu, hq, rows_h, want_out=True)
                     refs[hq] = (rows_h, (O, L))
             entry = {"B": wc.B, "S": wc.S, "Hq": wc.Hq, "Hkv": wc.Hkv, "D": wc.D,
@@ -494,7 +495,7 @@ def main():
                                             "mean_abs": max(e["mean_abs"] for e in errs),
                                             "lse_rel": max(e["lse_rel"] for e in errs),
                                             "within_tolerance": all(e["within"] for e in errs),
-                                            "rows": "12 rows x query heads %s" % (heads,)}
+                                            "rows": "rows 33, 64, 97, 127, 8 random, S-1; query heads %s" % (heads,)}
                 entry["p_terms%d" % pt] = rec
             if name in BWD_CONFIGS:
                 bms = max_over_ranks(cb.backward_ms(args.p_terms, 3, 1), world, dev)
