@@ -189,6 +189,18 @@ __device__ __forceinline__ void tld32(uint32_t taddr, float* r) {
         "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
       : "r"(taddr));
 }
+// The same load, also returning the maximum of the 32 values (tcgen05.ld.red, sm_103a).
+__device__ __forceinline__ void tld32_max(uint32_t taddr, float* r, float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]),
+        "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]),
+        "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]),
+        "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31]),
+        "=f"(mx)
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -540,31 +552,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       float v[128];
+      float bm[4];   // maxima of the four 32-key blocks
+      if constexpr (!DIAG) {
+        // every key of the tile is visible to every row: each load returns its block's maximum too
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tld32(tmem + lane_off + (sb ? T_S1 : T_S0) + 32 * c, v + 32 * c);
-      tmem_ld_wait();
-      if constexpr (DIAG) {   // keys after the row (key index = column inside the diagonal tile)
+        for (int c = 0; c < 4; ++c) tld32_max(tmem + lane_off + (sb ? T_S1 : T_S0) + 32 * c, v + 32 * c, bm[c]);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tld32(tmem + lane_off + (sb ? T_S1 : T_S0) + 32 * c, v + 32 * c);
+        tmem_ld_wait();
+        // keys after the row (key index = column inside the diagonal tile), then the block maxima
 #pragma unroll
         for (int k = 0; k < 128; ++k) v[k] = k > r ? -INFINITY : v[k];
-      }
-      // maxima of the four 32-key blocks and of the row
-      float bm[4];
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        const float* w = v + 32 * bb;
-        float c0 = fmax3(w[0], w[1], w[2]), c1 = fmax3(w[3], w[4], w[5]);
-        float c2 = fmax3(w[6], w[7], w[8]), c3 = fmax3(w[9], w[10], w[11]);
-        c0 = fmax3(c0, w[12], w[13]);
-        c1 = fmax3(c1, w[14], w[15]);
-        c2 = fmax3(c2, w[16], w[17]);
-        c3 = fmax3(c3, w[18], w[19]);
-        c0 = fmax3(c0, w[20], w[21]);
-        c1 = fmax3(c1, w[22], w[23]);
-        c2 = fmax3(c2, w[24], w[25]);
-        c3 = fmax3(c3, w[26], w[27]);
-        c0 = fmax3(c0, w[28], w[29]);
-        c1 = fmax3(c1, w[30], w[31]);
-        bm[bb] = fmax3(c0, c1, fmaxf(c2, c3));
+        for (int bb = 0; bb < 4; ++bb) {
+          const float* w = v + 32 * bb;
+          float c0 = fmax3(w[0], w[1], w[2]), c1 = fmax3(w[3], w[4], w[5]);
+          float c2 = fmax3(w[6], w[7], w[8]), c3 = fmax3(w[9], w[10], w[11]);
+          c0 = fmax3(c0, w[12], w[13]);
+          c1 = fmax3(c1, w[14], w[15]);
+          c2 = fmax3(c2, w[16], w[17]);
+          c3 = fmax3(c3, w[18], w[19]);
+          c0 = fmax3(c0, w[20], w[21]);
+          c1 = fmax3(c1, w[22], w[23]);
+          c2 = fmax3(c2, w[24], w[25]);
+          c3 = fmax3(c3, w[26], w[27]);
+          c0 = fmax3(c0, w[28], w[29]);
+          c1 = fmax3(c1, w[30], w[31]);
+          bm[bb] = fmax3(c0, c1, fmaxf(c2, c3));
+        }
       }
       const float mt = fmax3(bm[0], bm[1], fmaxf(bm[2], bm[3])) * sl2;
       const bool need = mt > m + RESCALE_LOG2;   // true at j = 0
