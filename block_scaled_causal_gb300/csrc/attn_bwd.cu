@@ -445,19 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     if (ok) ok = mbar_wait(bar(KB_Q), par, ctl, W_QD);
     ok = cta_all(ok);
     if (ok) ++q_seen;
-    if (ok) {
-      if (threadIdx.x < 32) rows_to_atom(smem + KV_SFQ, smem + KV_SFQA, min(BM, a.S - it * BM), threadIdx.x);
-      decode_rows(smem + KV_Q8, smem + KV_SFQ, smem + KV_Q, min(BM, a.S - it * BM));
-    }
+    if (ok && threadIdx.x < 32) rows_to_atom(smem + KV_SFQ, smem + KV_SFQA, min(BM, a.S - it * BM), threadIdx.x);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // S first: its scale factors occupy dP's first columns until it has completed
+    // S first (it reads the E4M3 bytes); its scale factors occupy dP's first columns until it has
+    // completed
     if (leader && ok) {
       mma_s(tmem, T_DP, sbase + KV_Q8, sbase + KV_K8, sbase + KV_SFQA, sbase + KV_SFKA);
       tc_commit(bar(KB_MMA1));
     }
+    // Q decoded to BF16 for the dK MMA while S computes (the previous dK MMA, the last reader of the
+    // BF16 tile, completed before this iteration)
+    if (ok) decode_rows(smem + KV_Q8, smem + KV_SFQ, smem + KV_Q, min(BM, a.S - it * BM));
     if (ok) ok = mbar_wait(bar(KB_MMA1), par, ctl, W_MMA1);
     ok = cta_all(ok);
     tc_fence_after();
