@@ -43,6 +43,8 @@ def _load():
     lib.mxfp8_quantize.argtypes = [ctypes.POINTER(QuantParams), vp]
     lib.bf16_attn_bwd.restype = i32
     lib.bf16_attn_bwd.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
+    lib.bf16_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.bf16_attn_bwd_workspace_bytes.argtypes = [i32, i32, i32]
     lib.bsc_read_device_status.restype = i32
     lib.bsc_read_device_status.argtypes = [vp, vp]
     return lib
@@ -103,6 +105,7 @@ class AttnBwdParams(ctypes.Structure):
         ("B", ctypes.c_int), ("S", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
         ("D", ctypes.c_int), ("layout", ctypes.c_int), ("softmax_scale", ctypes.c_float),
         ("dev_status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -252,10 +255,16 @@ def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=2, leaky=0, o=None
                                  o=o, lse=lse, stream=stream, o8_out=o8_out, bf16_out=bf16_out)
 
 
+def bf16_attn_bwd_workspace_bytes(B, S, Hq):
+    """Bytes of scratch the backward needs (the C call of the same name)."""
+    return int(lib.bf16_attn_bwd_workspace_bytes(B, S, Hq))
+
+
 def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softmax_scale=None, dq=None, dk=None,
-                  dv=None, dev_status=None, wait_timeout_ms=0, stream=None):
+                  dv=None, dev_status=None, wait_timeout_ms=0, stream=None, workspace=None):
     """Backward on decoded operands (quantised Q, K and token-normalised V, the forward's O, LSE);
-    returns (dQ, dK, dV) in bf16, laid out like q and k."""
+    returns (dQ, dK, dV) in bf16, laid out like q and k.  `workspace`: a device tensor of at least
+    bf16_attn_bwd_workspace_bytes(B, S, Hq) bytes, else one is allocated here."""
     B, S, Hq, D = _bshd_dims(q, layout)
     Hkv = _bshd_dims(k, layout)[2]
     if softmax_scale is None:
@@ -265,11 +274,15 @@ def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softma
     dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dk is None else dk
     dv = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dv is None else dv
+    ws_bytes = bf16_attn_bwd_workspace_bytes(B, S, Hq)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     p = AttnBwdParams(q=q.data_ptr(), q_sc=q_sc.data_ptr(), k=k.data_ptr(), k_sc=k_sc.data_ptr(),
                       vtn=vtn.data_ptr(), vtn_sc=vtn_sc.data_ptr(), o=o.data_ptr(), lse=lse.data_ptr(),
                       d_o=do.data_ptr(), dq=dq.data_ptr(), dk=dk.data_ptr(), dv=dv.data_ptr(), B=B, S=S, Hq=Hq,
                       Hkv=Hkv, D=D, layout=layout, softmax_scale=softmax_scale,
-                      dev_status=0 if dev_status is None else dev_status.data_ptr(), wait_timeout_ms=wait_timeout_ms)
+                      dev_status=0 if dev_status is None else dev_status.data_ptr(), wait_timeout_ms=wait_timeout_ms,
+                      workspace=workspace.data_ptr(), workspace_bytes=workspace.numel() * workspace.element_size())
     _check(lib.bf16_attn_bwd(ctypes.byref(p), _stream(stream)))
     return dq, dk, dv
 

@@ -299,6 +299,11 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
   return from_cuda(bsc::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t bf16_attn_bwd_workspace_bytes(int B, int S, int Hq) {
+  if (B <= 0 || S <= 0 || Hq <= 0) return 0;
+  return (size_t)2 * sizeof(float) * (size_t)B * (size_t)Hq * (size_t)((S + 127) / 128 * 128);
+}
+
 bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
   if (!p) return BSC_ERR_NULL;
   if (p->Hq < 0 || p->Hkv < 0) return BSC_ERR_SHAPE;
@@ -310,12 +315,13 @@ bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
   if (p->Hq % p->Hkv != 0) return BSC_ERR_SHAPE;
   if (!(std::isfinite(p->softmax_scale) && p->softmax_scale > 0.f)) return BSC_ERR_UNSUPPORTED;
   if (!p->q || !p->q_sc || !p->k || !p->k_sc || !p->vtn || !p->vtn_sc || !p->o || !p->lse || !p->d_o || !p->dq ||
-      !p->dk || !p->dv)
+      !p->dk || !p->dv || !p->workspace)
     return BSC_ERR_NULL;
-  const void* ptrs[] = {p->q, p->q_sc, p->k, p->k_sc, p->vtn, p->vtn_sc, p->o, p->lse, p->d_o, p->dq, p->dk, p->dv,
-                        p->dev_status};
+  const void* ptrs[] = {p->q,  p->q_sc, p->k,  p->k_sc, p->vtn,       p->vtn_sc,    p->o,
+                        p->lse, p->d_o, p->dq, p->dk,   p->dv, p->workspace, p->dev_status};
   for (const void* q : ptrs)
     if (!aligned16(q)) return BSC_ERR_ALIGN;
+  if (p->workspace_bytes < bf16_attn_bwd_workspace_bytes(p->B, p->S, p->Hq)) return BSC_ERR_SHAPE;
   if ((s = check_device()) != BSC_OK) return s;
 
   bsc::BwdArgs a;
@@ -335,6 +341,8 @@ bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
   a.dq = p->dq;
   a.dk = p->dk;
   a.dv = p->dv;
+  a.ws = p->workspace;
+  a.Sp = (p->S + 127) / 128 * 128;
   a.dev_status = p->dev_status;
   a.limit_ns = (unsigned long long)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
   a.B = p->B;

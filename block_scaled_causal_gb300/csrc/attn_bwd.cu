@@ -21,6 +21,7 @@
 // computes; the phases of an iteration run in turn, all threads taking part, thread 0 issuing the
 // copies and MMAs.  Every wait is bounded.
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -47,7 +48,10 @@ constexpr uint32_t T_S = 0, T_DP = 128, T_ACC0 = 256, T_ACC1 = 384;
 // (BF16, 64 columns), the A operands of the S and dP MMAs.
 constexpr uint32_t T_QT = 400, T_DOT = 432;
 
-enum Site : int { W_KV = 0x20, W_QD, W_MMA1, W_MMA2, W_MMA3, W_DO };
+enum Site : int {
+  W_KV = 0x20, W_QD, W_MMA1, W_MMA2, W_MMA3, W_DO, W_TMEM_BASE, W_PROD_S, W_PROD_QR, W_PROD_DK, W_DEC_KV, W_DEC_Q,
+  W_DEC_DK, W_SM_DO, W_SM_S, W_SM_DP,
+};
 
 // A wait's outcome made the same for every thread of the CTA (the TMEM loads are warp-collective).
 __device__ __forceinline__ bool cta_all(bool ok) { return __syncthreads_and(ok ? 1 : 0) != 0; }
@@ -84,64 +88,6 @@ __device__ __forceinline__ uint4 decode8(uint2 bytes, float scale) {
                        __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * scale);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Row statistics of the 128 query rows of tile `it`: LSE in log2 units and Dlt = <dO_i, O_i>.
-// Two threads per row, 64 head-dim elements each.  Rows past S get LSE = +inf and Dlt = 0, which
-// makes their P and dS exactly 0.
-__device__ __forceinline__ void row_stats(const BwdArgs& a, int b, int hq, int it, float* lse2, float* dlt) {
-  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
-  const int i = it * BM + r;
-  float acc = 0.f;
-  if (i < a.S) {
-    const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq : ((long long)i * a.B + b) * a.Hq + hq;
-    const uint4* po = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + row * HD + 64 * half);
-    const uint4* pd = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + row * HD + 64 * half);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 x = __ldg(po + c), y = __ldg(pd + c);
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
-        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
-      }
-    }
-  }
-  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-  if (half == 0) {
-    dlt[r] = i < a.S ? acc : 0.f;
-    lse2[r] = i < a.S ? a.lse[((long long)b * a.Hq + hq) * a.S + i] * 1.4426950408889634f : INFINITY;
-  }
-}
-
-// The same statistics from shared memory: the BF16 tiles of dO and O (TMA zero-fills rows past
-// S) and the tile's LSE values (copied for the rows below S only).
-__device__ __forceinline__ void row_stats_tiles(const BwdArgs& a, int it, const uint8_t* do_tile,
-                                                const uint8_t* o_tile, const float* lse_tile, float* lse2,
-                                                float* dlt) {
-  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
-  const int i = it * BM + r;
-  float acc = 0.f;
-  if (i < a.S) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t off = bf_off((uint32_t)r, (uint32_t)(64 * half + 8 * c));
-      const uint4 x = *reinterpret_cast<const uint4*>(o_tile + off);
-      const uint4 y = *reinterpret_cast<const uint4*>(do_tile + off);
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
-        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
-      }
-    }
-  }
-  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-  if (half == 0) {
-    dlt[r] = i < a.S ? acc : 0.f;
-    lse2[r] = i < a.S ? lse_tile[r] * 1.4426950408889634f : INFINITY;
-  }
 }
 
 // E4M3 tile [row][d] (TMA, 128-byte swizzle) with compact row scales -> BF16 [row][d].  Rows at
@@ -204,18 +150,6 @@ __device__ __forceinline__ void mma_bf16_k128(uint32_t d_tmem, uint32_t a_smem, 
     mma_f16_ss(d_tmem, da, db, idesc, (accumulate || s > 0) ? 1u : 0u);
   }
 }
-// S = Qh Kh^T from E4M3 tiles and row-atom scales (copied to TMEM columns t_sf.. first).
-__device__ __forceinline__ void mma_s(uint32_t tmem, uint32_t t_sf, uint32_t q8, uint32_t k8, uint32_t sfq,
-                                      uint32_t sfk) {
-  tc_cp_32x128b_warpx4(tmem + t_sf, desc_sf_block(sfq));
-  tc_cp_32x128b_warpx4(tmem + t_sf + 4, desc_sf_block(sfk));
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    mma_mxf8_ss(tmem + T_S, desc_kmajor_sw128(q8 + kk * 32), desc_kmajor_sw128(k8 + kk * 32),
-                idesc_mxf8(BM, BN, kk, kk), tmem + t_sf, tmem + t_sf + 4, kk > 0 ? 1u : 0u);
-  }
-}
-
 // S = Qh Kh^T with the Q bytes in tensor memory (columns t_q..t_q+31).
 __device__ __forceinline__ void mma_s_tq(uint32_t tmem, uint32_t t_sf, uint32_t t_q, uint32_t k8, uint32_t sfq,
                                          uint32_t sfk) {
@@ -277,17 +211,6 @@ __device__ __forceinline__ void compute_ds(uint32_t tmem, const RowView& rv, con
     }
   }
 }
-// A thread's 64 values as BF16 into a [q][key] tile: keys 8k + 2qd and 8k + 2qd + 1 are adjacent,
-// one 32-bit store per pair.
-__device__ __forceinline__ void store_rows(uint8_t* tile, const RowView& rv, const float (&x)[64]) {
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int key = 8 * k + 2 * rv.qd;
-    *reinterpret_cast<uint32_t*>(tile + bf_off(rv.ra, key)) = pack_bf16x2(x[4 * k], x[4 * k + 1]);
-    *reinterpret_cast<uint32_t*>(tile + bf_off(rv.rb, key)) = pack_bf16x2(x[4 * k + 2], x[4 * k + 3]);
-  }
-}
-
 // dS as BF16 into tensor memory (64 columns from t_ds), the A operand of dQ += dS K: register
 // 4c + 2rr + b of the 16x256b store (row ra or rb for rr = 0, 1; column 8c + 2qd + b) holds the
 // keys 16c + 8b + 2qd and the next, so column 8c + 2qd + b carries K positions 16c + 4qd + 2b + e
@@ -335,27 +258,173 @@ __device__ __forceinline__ void store_acc(uint32_t tmem_acc, void* out, const Bw
 }
 
 // ================================================================================================
-// dK, dV.  Shared memory (bytes from a 1024-aligned base):
-constexpr uint32_t KV_K8 = 0;                 // K bytes [key][d], swizzled
-constexpr uint32_t KV_V = KV_K8 + 16384;      // V bf16 [key][d]
-constexpr uint32_t KV_Q8 = KV_V + 32768;      // Q bytes [q][d], swizzled
-constexpr uint32_t KV_Q = KV_Q8 + 16384;      // Q bf16 [q][d]
-constexpr uint32_t KV_DO = KV_Q + 32768;      // dO bf16 [q][d]
-constexpr uint32_t KV_P = KV_DO + 32768;      // P bf16 [q][key] (the V bytes [key][d] before that)
-constexpr uint32_t KV_VN8 = KV_P;
-constexpr uint32_t KV_DS = KV_P + 32768;      // dS bf16 [q][key] (O bf16 [q][d] before that)
-constexpr uint32_t KV_SFQ = KV_DS + 32768;     // compact Q scales of the tile
-constexpr uint32_t KV_SFK = KV_SFQ + 512;      // compact K scales
-constexpr uint32_t KV_SFQA = KV_SFK + 512;     // the same as scale-factor atoms
-constexpr uint32_t KV_SFKA = KV_SFQA + 512;
-constexpr uint32_t KV_AMP = KV_SFKA + 512;
-constexpr uint32_t KV_STAT = KV_AMP + 128;    // [2 buffers][LSE | Dlt][128] floats
-constexpr uint32_t KV_LSE = KV_STAT + 2048;
-constexpr uint32_t KV_BAR = KV_LSE + 512;
-constexpr uint32_t KV_MISC = KV_BAR + 64;
+// Row statistics of the backward, once per call: Dlt_i = <dO_i, O_i> and LSE_i * log2(e) of every
+// query row into the workspace, two planes [B][Hq][Sp] of fp32 (Sp = 128 * ceil(S / 128)).  Rows
+// at or past S get Dlt = 0 and +inf, which make their P and dS exactly 0.  One warp per row.
+__global__ void __launch_bounds__(256) attn_bwd_stats_kernel(const __grid_constant__ BwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)a.B * a.Hq * a.Sp;
+  const long long rid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (rid >= rows) return;
+  const int i = (int)(rid % a.Sp);
+  const long long bh = rid / a.Sp;
+  const int hq = (int)(bh % a.Hq), b = (int)(bh / a.Hq);
+  float acc = 0.f;
+  if (i < a.S) {
+    const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq : ((long long)i * a.B + b) * a.Hq + hq;
+    const uint2 x = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + row * HD) + lane);
+    const uint2 y = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + row * HD) + lane);
+    const uint32_t xs[2] = {x.x, x.y}, ys[2] = {y.x, y.y};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+      acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if (lane == 0) {
+    a.ws[rid] = i < a.S ? acc : 0.f;
+    a.ws[rows + rid] = i < a.S ? a.lse[bh * a.S + i] * 1.4426950408889634f : INFINITY;
+  }
+}
+
+// E4M3 -> BF16 without the conversion unit.  A byte's sign placed at bit 15 and its seven other
+// bits (exponent and mantissa) at bits 4-10 of a BF16 give the byte's value times 2^-120 for every
+// code, subnormals included: the BF16 exponent field then holds the E4M3 one, whose bias is 120
+// less, and BF16 subnormals continue the E4M3 subnormal spacing.  Two exact BF16 multiplications
+// (2^120, then the block's power-of-two scale) finish the decode.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+  return r;
+}
+// t holds two bytes at bits 0-7 and 16-23 (other bits zero) -> BF16x2 of their values x 2^-120.
+__device__ __forceinline__ uint32_t e4m3x2_times_2m120(uint32_t t) {
+  const uint32_t u = t << 4;                  // magnitude bits at 4-10, sign at bit 11
+  const uint32_t sgn = u & 0x08000800u;
+  return u + sgn * 15u;                       // the sign moves from bit 11 to bit 15
+}
+// BF16x2 of the E8M0 scale 2^(sb - 127) (sb = 0: 2^-127, a BF16 subnormal).
+__device__ __forceinline__ uint32_t bf16x2_pow2_e8m0(uint32_t sb) {
+  const uint32_t h = sb == 0 ? 0x0040u : (sb << 7);
+  return h | (h << 16);
+}
+// Eight E4M3 bytes (one uint2, element e in byte e) times scale2 (BF16x2) -> eight BF16 (one uint4).
+__device__ __forceinline__ uint4 decode8_bf16(uint2 bytes, uint32_t scale2) {
+  constexpr uint32_t kTwo120 = 0x7B807B80u;   // 2^120 in both halves
+  uint32_t w[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t x = h ? bytes.y : bytes.x;
+    w[2 * h] = bf16x2_mul(bf16x2_mul(e4m3x2_times_2m120(__byte_perm(x, 0u, 0x4140)), kTwo120), scale2);
+    w[2 * h + 1] = bf16x2_mul(bf16x2_mul(e4m3x2_times_2m120(__byte_perm(x, 0u, 0x4342)), kTwo120), scale2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// A 128 x 128 E4M3 tile -> BF16 [row][d] (two 64-column blocks, 128-byte swizzle) by `nthr`
+// threads (index t).  Source rows are 128 bytes, swizzled (SW = true, as TMA writes a Q or K tile)
+// or plain (the token-normalised V tile); scale of (row r, 32-element block c) is
+// row_scale(r, c).  Each thread keeps one 8-element column position and walks rows nthr/16 apart.
+template <bool SW, int NTHR, typename RowScale>
+__device__ __forceinline__ void decode_tile_bf16(const uint8_t* src, uint8_t* dst, int t, RowScale row_scale) {
+  constexpr int kUnits = BM * (HD / 8) / NTHR;   // eight-element units per thread
+  constexpr int kBatch = 16;
+  static_assert(kUnits % kBatch == 0, "batches");
+  const int d0 = (t & 15) * 8, r0 = t >> 4;
+#pragma unroll 1
+  for (int u0 = 0; u0 < kUnits; u0 += kBatch) {
+    uint2 bytes[kBatch];
+    uint32_t sc[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {   // every load of the batch first
+      const int r = r0 + (NTHR / 16) * (u0 + u);
+      bytes[u] = *reinterpret_cast<const uint2*>(src + (SW ? sw(r, d0) : (uint32_t)(r * HD + d0)));
+      sc[u] = row_scale(r, d0 >> 5);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = r0 + (NTHR / 16) * (u0 + u);
+      *reinterpret_cast<uint4*>(dst + bf_off(r, d0)) = decode8_bf16(bytes[u], sc[u]);
+    }
+  }
+}
+
+// ================================================================================================
+// dK, dV.  One CTA per (batch, KV head, 128-key tile jt); it walks the pairs n = 0..N-1 of (query
+// head of the group, query tile at or after jt): query tiles from the last down, the group's heads
+// innermost, so that CTAs of one KV head running at the same time read the same Q and dO tiles from
+// L2.  The keys sit on the TMEM lanes, so P^T and dS^T are the A operands of the dV and dK MMAs
+// straight from tensor memory:
+//   S^T  = Kh Qh^T      block-scaled E4M3 MMA on the bytes (A = K, B = Q, both K-major)
+//   dP^T = Vt dO^T      BF16 (A = Vt [key][d], B = dO [q][d], both K-major)
+//   P^T  = exp2(S^T scale log2(e) - LSE2[q]),  dS^T = P^T (dP^T - Dlt[q])     (softmax warps)
+//   dV  += P^T dO       A = P^T (BF16 over the first 64 columns of S^T), B = dO read along q
+//   dK  += dS^T Qh      A = dS^T (BF16 over the first 64 columns of dP^T), B = decoded Q along q
+// Roles (8 warps): warp 0 lane 0 issues the copies; warp 1 lane 0 issues the MMAs in the order
+//   S(0) dP(0) | dV(n) S(n+1) dK(n) dP(n+1) | ...
+// so that the softmax of pair n + 1 runs under dK(n) and dP(n + 1); warps 2-3 decode (V once, the Q
+// bytes of every pair to BF16, the scale atoms); warps 4-7 compute P and dS, one key row per
+// thread.  TMEM: S^T 0-127, dP^T 128-255, dV 256-383, dK 384-511.  The S MMA's scale factors sit in
+// dP^T's columns 120-127: the softmax reads those columns of dP^T(n) before it releases P(n), after
+// which S(n + 1) is issued.  An MMA that rewrites columns an earlier one reads (S(n+1) over P^T(n),
+// dP(n+1) over dS^T(n) and the scale factors) is issued after it: the MMAs of one thread run in
+// issue order.  The MMA-issuing thread waits on named barriers only (an mbarrier wait there drains
+// its MMAs in flight).
+//
+// Shared memory (bytes from a 1024-aligned base):
+constexpr uint32_t KV_K8 = 0;                    // K bytes [key][d], swizzled
+constexpr uint32_t KV_V = KV_K8 + 16384;         // V bf16 [key][d]
+constexpr uint32_t KV_Q8 = KV_V + 32768;         // 2 stages: Q bytes [q][d], swizzled
+constexpr uint32_t KV_Q = KV_Q8 + 2 * 16384;     // 2 stages: decoded Q bf16 [q][d]
+constexpr uint32_t KV_VN8 = KV_Q + 32768;        // V bytes [key][d], in Q stage 1 before its first use
+constexpr uint32_t KV_DO = KV_Q + 2 * 32768;     // 2 stages: dO bf16 [q][d]
+constexpr uint32_t KV_SFQ = KV_DO + 2 * 32768;   // 2 stages: compact Q scales
+constexpr uint32_t KV_SFK = KV_SFQ + 1024;       // compact K scales
+constexpr uint32_t KV_SFQA = KV_SFK + 512;       // 2 stages: Q scale atoms
+constexpr uint32_t KV_SFKA = KV_SFQA + 1024;     // K scale atom
+constexpr uint32_t KV_AMP = KV_SFKA + 512;       // V token amplitudes
+constexpr uint32_t KV_STAT = KV_AMP + 128;       // 2 stages: Dlt[128], then LSE2[128]
+constexpr uint32_t KV_BAR = KV_STAT + 2048;
+constexpr uint32_t KV_MISC = KV_BAR + 128;       // TMEM slot, abort flag
 constexpr uint32_t KV_SMEM = KV_MISC + 16 + 1024;
 static_assert(KV_SMEM <= 227 * 1024, "shared memory budget");
-enum KvBar : uint32_t { KB_KV = 0, KB_Q, KB_DO, KB_MMA1, KB_MMA2, KB_MMA3, KB_DRAIN, KB_COUNT };
+constexpr uint32_t T_ST = 0, T_DPT = 128, T_DV = 256, T_DK = 384;
+constexpr uint32_t T_SFK = T_DPT + 120, T_SFQ = T_DPT + 124;
+// mbarriers:
+//   KV         K, its scales, the V bytes and amplitudes landed
+//   QF + st    Q bytes and compact scales of stage st landed
+//   DF + st    dO and the row statistics of stage st landed
+//   SF + n%2   S^T(n) computed (and every MMA issued before it)
+//   DP         dP^T(n) computed
+//   DK + n%2   dK(n) computed (and every MMA issued before it)
+//   QR + st    the decoders are done with Q stage st (count 2: one arrival per decoder warp)
+enum KvBar : uint32_t {
+  KB_KV = 0,
+  KB_QF = 1,
+  KB_DF = KB_QF + 2,
+  KB_SF = KB_DF + 2,
+  KB_DP = KB_SF + 2,
+  KB_DK,
+  KB_QR = KB_DK + 2,
+  KB_DRAIN = KB_QR + 2,
+  KB_COUNT
+};
+static_assert(KB_COUNT * 8 <= 128, "barrier slots");
+// Named barriers (each with the MMA warp):
+//   NB_KV        decoders: the K scale atom and the BF16 V tile are written (once)
+//   NB_Q + n%2   decoders: the Q scale atom of pair n is written
+//   NB_QD + n%2  decoders: the BF16 Q of pair n is written
+//   NB_DO        softmax: dO of pair n landed
+//   NB_P         softmax: P^T(n) is in TMEM, and columns 96-127 of dP^T(n) are read
+//   NB_DS        softmax: dS^T(n) is in TMEM
+// The decoders block on NB_QD and the softmax warps on NB_DS, and arrive on the others: each
+// blocking generation they pass shows the MMA warp has passed the previous generation of every
+// barrier they arrive on next, so no generation ever holds arrivals of two pairs, also once a role
+// has given up (failed wait: it skips its work but meets every generation).  Both meet their
+// generations in the MMA warp's order (the decoders Q(n+1) before QD(n)), so none waits forever.
+constexpr uint32_t NB_KV = 1, NB_Q = 2, NB_QD = 4, NB_DO = 6, NB_P = 7, NB_DS = 8, NB_DEC = 9;
+constexpr uint32_t kNbDec = 96, kNbSm = 160;
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -364,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   auto bar = [&](uint32_t i) { return sbase + KV_BAR + 8u * i; };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + KV_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_MISC + 4);
-  auto stat = [&](int buf) { return reinterpret_cast<float*>(smem + KV_STAT) + buf * 256; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int T = (a.S + BN - 1) / BN;
   const int g = a.Hq / a.Hkv;
@@ -374,154 +443,316 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   const int hk = bh % a.Hkv, b = bh / a.Hkv;
   const long long kv_plane = (long long)b * a.Hkv + hk;
   const int nkeys = min(BN, a.S - jt * BN);
-  const int n_iter = g * (T - jt);   // (query head, query tile) pairs
+  const int N = g * (T - jt);   // pairs; the last g of them are the diagonal tile
+  auto hq_of = [&](int n) { return hk * g + n % g; };
+  auto it_of = [&](int n) { return T - 1 - n / g; };
 
   if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < KB_COUNT; ++i) mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < KB_COUNT; ++i) mbar_init(bar(i), (i == KB_QR || i == KB_QR + 1) ? 2u : 1u);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if ((threadIdx.x >> 5) == 0) {
+  if (warp == 0) {
     tmem_alloc(sbase + KV_MISC, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // The CTA holds all 512 columns, so the allocation starts at column 0 and every TMEM address is
+  // a compile-time constant.  Checked: a different base aborts the call.
+  constexpr uint32_t tmem = 0;
+  if (threadIdx.x == 0 && *tmem_slot != 0u) {
+    *abort_flag = 1;
+    if (a.dev_status) atomicCAS(a.dev_status, 0, 0x100 | W_TMEM_BASE);
+  }
+  __syncthreads();
+  const bool start_ok = *abort_flag == 0;
   const WaitCtl ctl{abort_flag, a.dev_status, a.limit_ns};
-  const bool leader = threadIdx.x == 0;
-  // Query tiles from the last down to the key tile, the group's heads innermost: CTAs of one KV head
-  // that run at the same time then read the same Q, dO and O tiles, which stay in L2.
-  auto hq_of = [&](int n) { return hk * g + n % g; };
-  auto it_of = [&](int n) { return T - 1 - n / g; };
-  auto load_q = [&](int n) {
-    const uint32_t nr = (uint32_t)min(BM, a.S - it_of(n) * BM);
-    mbar_arrive_expect_tx(bar(KB_Q), BM * HD + 4 * nr);
-    tma_load_4d(sbase + KV_Q8, &a.tm_q, bar(KB_Q), 0, hq_of(n), it_of(n) * BM, b);
-    bulk_load(sbase + KV_SFQ, a.q_sc + (((long long)b * a.Hq + hq_of(n)) * a.S + (long long)it_of(n) * BM) * 4, 4 * nr,
-              bar(KB_Q));
-  };
-  // dO into its tile and O into the dS tile (read for the row statistics before dS is written)
-  auto load_do = [&](int n) {
-    const int it = it_of(n);
-    const uint32_t lse_bytes = 4u * (uint32_t)min(BM, a.S - it * BM);
-    mbar_arrive_expect_tx(bar(KB_DO), 4 * BM * HD + lse_bytes);
-    tma_load_4d(sbase + KV_DO, &a.tm_do, bar(KB_DO), 0, hq_of(n), it * BM, b);
-    tma_load_4d(sbase + KV_DO + ATOM, &a.tm_do, bar(KB_DO), 64, hq_of(n), it * BM, b);
-    tma_load_4d(sbase + KV_DS, &a.tm_o, bar(KB_DO), 0, hq_of(n), it * BM, b);
-    tma_load_4d(sbase + KV_DS + ATOM, &a.tm_o, bar(KB_DO), 64, hq_of(n), it * BM, b);
-    bulk_load(sbase + KV_LSE, a.lse + ((long long)b * a.Hq + hq_of(n)) * a.S + (long long)it * BM, lse_bytes,
-              bar(KB_DO));
-  };
-  bool ok = true;
-  int q_issued = 0, q_seen = 0, do_issued = 0, do_seen = 0;
 
-  // this CTA's K and V tiles, and the first query tile
-  if (leader) {
-    mbar_arrive_expect_tx(bar(KB_KV), 2 * BN * HD + 4 * (uint32_t)nkeys + (uint32_t)nkeys);
-    tma_load_4d(sbase + KV_K8, &a.tm_k, bar(KB_KV), 0, hk, jt * BN, b);
-    bulk_load(sbase + KV_SFK, a.k_sc + (kv_plane * a.S + (long long)jt * BN) * 4, 4 * (uint32_t)nkeys, bar(KB_KV));
-    tma_load_4d(sbase + KV_VN8, &a.tm_vtn, bar(KB_KV), 0, hk, jt * BN, b);
-    bulk_load(sbase + KV_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, (uint32_t)nkeys, bar(KB_KV));
-    load_q(0);
-    load_do(0);
-  }
-  q_issued = do_issued = 1;
-  ok = cta_all(mbar_wait(bar(KB_KV), 0, ctl, W_KV));
-  const bool kv_seen = ok;
-  if (ok) {
-    if (threadIdx.x < 32) rows_to_atom(smem + KV_SFK, smem + KV_SFKA, nkeys, threadIdx.x);
-    decode_vt(smem + KV_VN8, smem + KV_AMP, smem + KV_V, nkeys);
-  }
-  __syncthreads();   // the V bytes are read before P overwrites them
-
-  const RowView rv = row_view();
-  for (int n = 0; n < n_iter; ++n) {
-    const uint32_t par = (uint32_t)n & 1u;
-    const int it = it_of(n);
-    float* lse2 = stat(n & 1);
-    float* dlt = lse2 + 128;
-    if (ok) ok = mbar_wait(bar(KB_Q), par, ctl, W_QD);
-    ok = cta_all(ok);
-    if (ok) ++q_seen;
-    if (ok && threadIdx.x < 32) rows_to_atom(smem + KV_SFQ, smem + KV_SFQA, min(BM, a.S - it * BM), threadIdx.x);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // S first (it reads the E4M3 bytes); its scale factors occupy dP's first columns until it has
-    // completed
-    if (leader && ok) {
-      mma_s(tmem, T_DP, sbase + KV_Q8, sbase + KV_K8, sbase + KV_SFQA, sbase + KV_SFKA);
-      tc_commit(bar(KB_MMA1));
-    }
-    // Q decoded to BF16 for the dK MMA while S computes (the previous dK MMA, the last reader of the
-    // BF16 tile, completed before this iteration)
-    if (ok) decode_rows(smem + KV_Q8, smem + KV_SFQ, smem + KV_Q, min(BM, a.S - it * BM));
-    if (ok) ok = mbar_wait(bar(KB_MMA1), par, ctl, W_MMA1);
-    ok = cta_all(ok);
-    tc_fence_after();
-    if (ok) ok = mbar_wait(bar(KB_DO), par, ctl, W_DO);
-    ok = cta_all(ok);
-    if (ok) ++do_seen;
-    if (leader && ok) {
-      if (n + 1 < n_iter) {   // the Q bytes are free again: fetch the next query tile's
-        load_q(n + 1);
-        ++q_issued;
+  if (warp == 0) {
+    // ======================= copies
+    if (lane == 0) {
+      prefetch_tensormap(&a.tm_q);
+      prefetch_tensormap(&a.tm_k);
+      prefetch_tensormap(&a.tm_vtn);
+      prefetch_tensormap(&a.tm_do);
+      const long long ws_plane = (long long)a.B * a.Hq * a.Sp;
+      auto load_q = [&](int n) {
+        const int st = n & 1, it = it_of(n), hq = hq_of(n);
+        const uint32_t nr = (uint32_t)min(BM, a.S - it * BM);
+        mbar_arrive_expect_tx(bar(KB_QF + st), BM * HD + 4 * nr);
+        tma_load_4d(sbase + KV_Q8 + st * 16384, &a.tm_q, bar(KB_QF + st), 0, hq, it * BM, b);
+        bulk_load(sbase + KV_SFQ + st * 512, a.q_sc + (((long long)b * a.Hq + hq) * a.S + (long long)it * BM) * 4,
+                  4 * nr, bar(KB_QF + st));
+      };
+      auto load_do = [&](int n) {
+        const int st = n & 1, it = it_of(n), hq = hq_of(n);
+        const long long srow = ((long long)b * a.Hq + hq) * a.Sp + (long long)it * BM;
+        mbar_arrive_expect_tx(bar(KB_DF + st), 2 * BM * HD + 1024);
+        tma_load_4d(sbase + KV_DO + st * 32768, &a.tm_do, bar(KB_DF + st), 0, hq, it * BM, b);
+        tma_load_4d(sbase + KV_DO + st * 32768 + ATOM, &a.tm_do, bar(KB_DF + st), 64, hq, it * BM, b);
+        bulk_load(sbase + KV_STAT + st * 1024, a.ws + srow, 512, bar(KB_DF + st));
+        bulk_load(sbase + KV_STAT + st * 1024 + 512, a.ws + ws_plane + srow, 512, bar(KB_DF + st));
+      };
+      bool ok = start_ok;
+      int nq[2] = {0, 0}, nd[2] = {0, 0};
+      if (ok) {
+        mbar_arrive_expect_tx(bar(KB_KV), 2 * BN * HD + 4 * (uint32_t)nkeys + (uint32_t)nkeys);
+        tma_load_4d(sbase + KV_K8, &a.tm_k, bar(KB_KV), 0, hk, jt * BN, b);
+        bulk_load(sbase + KV_SFK, a.k_sc + (kv_plane * a.S + (long long)jt * BN) * 4, 4 * (uint32_t)nkeys,
+                  bar(KB_KV));
+        tma_load_4d(sbase + KV_VN8, &a.tm_vtn, bar(KB_KV), 0, hk, jt * BN, b);
+        bulk_load(sbase + KV_AMP, a.vtn_sc + kv_plane * a.S + (long long)jt * BN, (uint32_t)nkeys, bar(KB_KV));
+        for (int n = 0; n < 2 && n < N; ++n) {
+          load_q(n);
+          load_do(n);
+          nq[n] = nd[n] = 1;
+        }
       }
-      mma_bf16_k128<false, false>(tmem + T_DP, sbase + KV_DO, sbase + KV_V, false);   // dP = dO V^T
-      tc_commit(bar(KB_MMA3));
+      // Stage n % 2 takes pair n + 2 once pair n is done with it: the Q bytes after S^T(n) and the
+      // decode of Q(n); dO and the statistics after dK(n) (the softmax has used them by then).
+      for (int n = 0; ok && n + 2 < N; ++n) {
+        const int st = n & 1;
+        const uint32_t ph = (uint32_t)(n >> 1) & 1u;
+        if (!(ok = mbar_wait(bar(KB_SF + st), ph, ctl, W_PROD_S))) break;
+        if (!(ok = mbar_wait(bar(KB_QR + st), ph, ctl, W_PROD_QR))) break;
+        load_q(n + 2);
+        ++nq[st];
+        if (!(ok = mbar_wait(bar(KB_DK + st), ph, ctl, W_PROD_DK))) break;
+        load_do(n + 2);
+        ++nd[st];
+      }
+      // every copy this thread issued lands before the CTA may exit
+      if (start_ok) mbar_wait_drain(bar(KB_KV), 0, a.limit_ns);
+      for (int st = 0; st < 2; ++st) {
+        if (nq[st] > 0) mbar_wait_drain(bar(KB_QF + st), (uint32_t)(nq[st] - 1) & 1u, a.limit_ns);
+        if (nd[st] > 0) mbar_wait_drain(bar(KB_DF + st), (uint32_t)(nd[st] - 1) & 1u, a.limit_ns);
+      }
     }
-    // LSE and Dlt of this query tile while dP computes (dO and O are in shared memory by now)
-    if (ok) row_stats_tiles(a, it, smem + KV_DO, smem + KV_DS, reinterpret_cast<const float*>(smem + KV_LSE), lse2, dlt);
-    __syncthreads();   // O's tile is read before dS overwrites it
-    float p[64];
-    if (ok) {
-      compute_p(tmem, rv, lse2, a.scale_log2e, it == jt, p);
-      store_rows(smem + KV_P, rv, p);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================= MMA issuer: lane 0 issues, the whole warp meets the named barriers
+    const bool ok = start_ok;
+    auto live = [&]() { return ok && *abort_flag == 0; };
+    const uint64_t dK8 = desc_kmajor_sw128(sbase + KV_K8), dQ8 = desc_kmajor_sw128(sbase + KV_Q8);
+    const uint64_t dVk = desc_kmajor_sw128(sbase + KV_V), dDOk = desc_kmajor_sw128(sbase + KV_DO);
+    const uint64_t dDOm = smem_desc(sbase + KV_DO, ATOM, 1024, 2), dQm = smem_desc(sbase + KV_Q, ATOM, 1024, 2);
+    constexpr uint32_t idS = idesc_mxf8(BN, BM, 0, 0);
+    constexpr uint32_t idP = idesc_bf16(BN, BM), idMN = idesc_bf16(BN, HD) | (1u << 16);
+    auto issue_s = [&](int n) {   // S^T = K Q^T (block-scaled)
+      const uint32_t st = (uint32_t)n & 1u;
+      tc_cp_32x128b_warpx4(tmem + T_SFK, desc_sf_block(sbase + KV_SFKA));
+      tc_cp_32x128b_warpx4(tmem + T_SFQ, desc_sf_block(sbase + KV_SFQA + 512 * st));
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_mxf8_ss(tmem + T_ST, dK8 + 2 * kk, dQ8 + st * (16384 >> 4) + 2 * kk,
+                    idS | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), tmem + T_SFK, tmem + T_SFQ, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(KB_SF + st));
+    };
+    auto issue_dp = [&](int n) {  // dP^T = V dO^T
+      const uint64_t db = dDOk + ((uint32_t)n & 1u) * (32768 >> 4);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t off = ((s >> 2) * ATOM + (s & 3) * 32) >> 4;
+        mma_f16_ss(tmem + T_DPT, dVk + off, db + off, idP, s > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(KB_DP));
+    };
+    auto issue_dv = [&](int n) {  // dV += P^T dO
+      const uint64_t db = dDOm + ((uint32_t)n & 1u) * (32768 >> 4);
+      const uint32_t acc0 = n > 0 ? 1u : 0u;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) mma_f16_ts(tmem + T_DV, tmem + T_ST + 8 * s, db + s * (2048 >> 4), idMN, s > 0 ? 1u : acc0);
+    };
+    auto issue_dk = [&](int n) {  // dK += dS^T Q
+      const uint64_t db = dQm + ((uint32_t)n & 1u) * (32768 >> 4);
+      const uint32_t acc0 = n > 0 ? 1u : 0u;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) mma_f16_ts(tmem + T_DK, tmem + T_DPT + 8 * s, db + s * (2048 >> 4), idMN, s > 0 ? 1u : acc0);
+      tc_commit(bar(KB_DK + ((uint32_t)n & 1u)));
+    };
+    named_sync(NB_KV, kNbDec);
+    named_sync(NB_Q + 0, kNbDec);
+    if (lane == 0 && live()) {
+      tc_fence_after();
+      issue_s(0);
     }
-    if (ok) ok = mbar_wait(bar(KB_MMA3), par, ctl, W_MMA3);
-    ok = cta_all(ok);
-    tc_fence_after();
+    __syncwarp();
+    named_sync(NB_DO, kNbSm);
+    if (lane == 0 && live()) {
+      tc_fence_after();
+      issue_dp(0);
+    }
+    __syncwarp();
+    for (int n = 0; n < N; ++n) {
+      named_sync(NB_P, kNbSm);
+      if (lane == 0 && live()) {
+        tc_fence_after();
+        issue_dv(n);
+      }
+      __syncwarp();
+      if (n + 1 < N) {
+        named_sync(NB_Q + ((n + 1) & 1), kNbDec);
+        if (lane == 0 && live()) {
+          tc_fence_after();
+          issue_s(n + 1);
+        }
+        __syncwarp();
+      }
+      named_sync(NB_QD + (n & 1), kNbDec);
+      named_sync(NB_DS, kNbSm);
+      if (lane == 0 && live()) {
+        tc_fence_after();
+        issue_dk(n);
+      }
+      __syncwarp();
+      if (n + 1 < N) {
+        named_sync(NB_DO, kNbSm);
+        if (lane == 0 && live()) {
+          tc_fence_after();
+          issue_dp(n + 1);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) tc_commit(bar(KB_DRAIN));   // every MMA of the CTA
+    __syncwarp();
+  } else if (warp < 4) {
+    // ======================= decoders (64 threads): the K scale atom and BF16 V once, then per
+    // pair the Q scale atom (one pair ahead) and the BF16 Q
+    const int t = threadIdx.x - 64;
+    bool ok = start_ok && __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_KV), 0, ctl, W_DEC_KV));
     if (ok) {
-      float ds[64];
-      compute_ds(tmem, rv, dlt, p, ds);
-      store_rows(smem + KV_DS, rv, ds);
+      if (warp == 2) rows_to_atom(smem + KV_SFK, smem + KV_SFKA, nkeys, lane);
+      const uint8_t* amp = smem + KV_AMP;
+      decode_tile_bf16<false, 64>(smem + KV_VN8, smem + KV_V, t, [&](int r, int) {
+        return r < nkeys ? bf16x2_pow2_e8m0(amp[r]) : 0u;
+      });
     }
     fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (leader && ok) {
-      mma_bf16_k128<true, true>(tmem + T_ACC0, sbase + KV_P, sbase + KV_DO, n > 0);   // dV += P^T dO
-      mma_bf16_k128<true, true>(tmem + T_ACC1, sbase + KV_DS, sbase + KV_Q, n > 0);   // dK += dS^T Q
-      tc_commit(bar(KB_MMA2));
+    named_sync(NB_DEC, 64);   // every V byte is read before Q stage 1 is written
+    named_arrive(NB_KV, kNbDec);
+    auto atom = [&](int n) {   // the Q scale atom of pair n, once its copy landed
+      const int st = n & 1;
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_QF + st), (uint32_t)(n >> 1) & 1u, ctl, W_DEC_Q));
+      if (ok && warp == 2) rows_to_atom(smem + KV_SFQ + st * 512, smem + KV_SFQA + st * 512, min(BM, a.S - it_of(n) * BM), lane);
+      fence_proxy_async_smem();
+      named_arrive(NB_Q + st, kNbDec);
+    };
+    atom(0);
+    for (int n = 0; n < N; ++n) {
+      const int st = n & 1;
+      if (n + 1 < N) atom(n + 1);
+      // Q stage st in BF16, once dK(n - 2), its last reader, has completed
+      if (n >= 2 && ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_DK + st), (uint32_t)((n - 2) >> 1) & 1u, ctl, W_DEC_DK));
+      if (ok) {
+        const int nr = min(BM, a.S - it_of(n) * BM);
+        const uint8_t* sfq = smem + KV_SFQ + st * 512;
+        decode_tile_bf16<true, 64>(smem + KV_Q8 + st * 16384, smem + KV_Q + st * 32768, t, [&](int r, int c) {
+          return r < nr ? bf16x2_pow2_e8m0(sfq[r * 4 + c]) : 0u;
+        });
+      }
+      fence_proxy_async_smem();
+      named_sync(NB_QD + st, kNbDec);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KB_QR + st));
     }
-    if (ok) ok = mbar_wait(bar(KB_MMA2), par, ctl, W_MMA2);
-    ok = cta_all(ok);
-    tc_fence_after();
-    if (leader && ok && n + 1 < n_iter) {   // dO is free again
-      load_do(n + 1);
-      ++do_issued;
-    }
+  } else {
+    // ======================= softmax: key row kr of the tile per thread
+    const int qq = warp & 3, kr = qq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const float sl2 = a.scale_log2e;
+    bool ok = start_ok;
+    // dS of 32 queries from their P, dP and Dlt, packed to BF16 pairs
+    auto ds_chunk = [&](const float* p, const float* d, const float* dlt, uint32_t* w) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 dl = *reinterpret_cast<const float2*>(dlt + 2 * i);
+        w[i] = pack_bf16x2(p[2 * i] * (d[2 * i] - dl.x), p[2 * i + 1] * (d[2 * i + 1] - dl.y));
+      }
+    };
+    auto pair = [&](int n, auto diag_tag) {
+      constexpr bool DIAG = decltype(diag_tag)::value;
+      const int st = n & 1;
+      const float* dlt = reinterpret_cast<const float*>(smem + KV_STAT + st * 1024);
+      const float* lse2 = dlt + 128;
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_DF + st), (uint32_t)(n >> 1) & 1u, ctl, W_SM_DO));
+      named_arrive(NB_DO, kNbSm);
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_SF + st), (uint32_t)(n >> 1) & 1u, ctl, W_SM_S));
+      float p[128];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tld32(tmem + lane_off + T_ST + 32 * c, p + 32 * c);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 32; ++q4) {
+          const float4 l = *reinterpret_cast<const float4*>(lse2 + 4 * q4);
+          const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = 4 * q4 + e;
+            const float x = ex2_approx(fmaf(p[q], sl2, -lv[e]));
+            p[q] = (DIAG && q < kr) ? 0.f : x;   // in the diagonal tile a query sees keys up to itself
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(p[32 * c + 2 * i], p[32 * c + 2 * i + 1]);
+          tst16(tmem + lane_off + T_ST + 16 * c, w);
+        }
+      }
+      uint32_t ds3[16];
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_DP), (uint32_t)n & 1u, ctl, W_SM_DP));
+      if (ok) {
+        tc_fence_after();
+        float d[32];
+        tld32(tmem + lane_off + T_DPT + 96, d);   // the columns the next S MMA's scales go into
+        tmem_ld_wait();
+        ds_chunk(p + 96, d, dlt + 96, ds3);
+        tmem_st_wait();
+        tc_fence_before();
+      }
+      named_arrive(NB_P, kNbSm);
+      if (ok) {
+        // dS^T of queries 32c.. goes over columns 16c.., which hold dP^T of queries read by then
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          float d[32];
+          uint32_t w[16];
+          tld32(tmem + lane_off + T_DPT + 32 * c, d);
+          tmem_ld_wait();
+          ds_chunk(p + 32 * c, d, dlt + 32 * c, w);
+          tst16(tmem + lane_off + T_DPT + 16 * c, w);
+          if (c == 1) tst16(tmem + lane_off + T_DPT + 48, ds3);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+      }
+      named_sync(NB_DS, kNbSm);
+    };
+    int n = 0;
+    for (; n < N - g; ++n) pair(n, std::false_type{});
+    for (; n < N; ++n) pair(n, std::true_type{});
   }
-  if (ok && n_iter > 0) {
-    store_acc(tmem + T_ACC0, a.dv, a, a.Hkv, b, hk, jt, 1.0f);
-    store_acc(tmem + T_ACC1, a.dk, a, a.Hkv, b, hk, jt, a.scale);
-  }
-  if (leader) {
-    // every tcgen05 operation and copy this thread issued must finish before the CTA exits
-    tc_commit(bar(KB_DRAIN));
-    mbar_wait_drain(bar(KB_DRAIN), 0, a.limit_ns);
-    if (!kv_seen) mbar_wait_drain(bar(KB_KV), 0, a.limit_ns);
-    if (q_issued > q_seen) mbar_wait_drain(bar(KB_Q), (uint32_t)(q_issued - 1) & 1u, a.limit_ns);
-    if (do_issued > do_seen) mbar_wait_drain(bar(KB_DO), (uint32_t)(do_issued - 1) & 1u, a.limit_ns);
+
+  // ======================= epilogue: dV and dK from TMEM, 8 warps
+  tc_fence_before();
+  __syncthreads();
+  const bool drained = mbar_wait_drain(bar(KB_DRAIN), 0, a.limit_ns);
+  tc_fence_after();
+  if (cta_all(drained && start_ok && *abort_flag == 0)) {
+    store_acc(tmem + T_DV, a.dv, a, a.Hkv, b, hk, jt, 1.0f);
+    store_acc(tmem + T_DK, a.dk, a, a.Hkv, b, hk, jt, a.scale);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if ((threadIdx.x >> 5) == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ================================================================================================
@@ -602,7 +833,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     load_kv(0);
   }
   kv_issued[0] = 1;
-  row_stats(a, b, hq, it, lse2, dlt);
+  if (threadIdx.x < BM) {   // the tile's row statistics, written by the statistics kernel
+    const long long srow = ((long long)b * a.Hq + hq) * a.Sp + (long long)it * BM + threadIdx.x;
+    dlt[threadIdx.x] = a.ws[srow];
+    lse2[threadIdx.x] = a.ws[(long long)a.B * a.Hq * a.Sp + srow];
+  }
   ok = cta_all(mbar_wait(bar(QB_QD), 0, ctl, W_QD));
   const bool qd_seen = ok;
   if (ok && threadIdx.x < 32) {
@@ -700,8 +935,12 @@ cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st) {
     attr_set = true;
   }
   const long long T = (args.S + BM - 1) / BM;
-  attn_bwd_dq_kernel<<<(unsigned)((long long)args.B * args.Hq * T), kThreads, QQ_SMEM, st>>>(args);
+  const long long rows = (long long)args.B * args.Hq * args.Sp;
+  attn_bwd_stats_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(args);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_bwd_dq_kernel<<<(unsigned)((long long)args.B * args.Hq * T), kThreads, QQ_SMEM, st>>>(args);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_bwd_dkdv_kernel<<<(unsigned)((long long)args.B * args.Hkv * T), kThreads, KV_SMEM, st>>>(args);
   return cudaGetLastError();

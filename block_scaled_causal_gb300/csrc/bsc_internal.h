@@ -70,9 +70,11 @@ struct BwdArgs {
   void* dq;             // bf16, Q's layout
   void* dk;             // bf16, K's layout
   void* dv;             // bf16, K's layout
+  float* ws;            // workspace: Dlt [B][Hq][Sp], then LSE * log2(e) [B][Hq][Sp]
   int32_t* dev_status;
   unsigned long long limit_ns;
   int B, S, Hq, Hkv, layout;
+  int Sp;               // S rounded up to the 128-row tile
   float scale, scale_log2e;
 };
 

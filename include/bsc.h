@@ -237,6 +237,13 @@ typedef struct {
   float softmax_scale;    /* finite and > 0, else BSC_ERR_UNSUPPORTED */
   int32_t* dev_status;    /* optional, as in bsc_attn_fwd_params */
   uint32_t wait_timeout_ms;
+  /* [scratch] device memory of at least bf16_attn_bwd_workspace_bytes(B, S, Hq) bytes, 16-byte
+   * aligned, overlapping no other argument; owned by the caller, contents on entry ignored,
+   * on return undefined.  The call writes the per-row statistics of the backward there (Dlt_i and
+   * LSE_i*log2(e), fp32, rows padded to a multiple of 128) once, for both backward kernels.
+   * NULL: BSC_ERR_NULL; workspace_bytes below the required size: BSC_ERR_SHAPE. */
+  float* workspace;
+  size_t workspace_bytes;
 } bsc_attn_bwd_params;
 
 /*
@@ -247,9 +254,15 @@ typedef struct {
  * keys j <= i: P = exp(s - LSE), dV = P^T dO, dP = dO.Vt^T, Dlt_i = <dO_i, O_i>,
  * dS = P*(dP - Dlt), dQ = scale*dS.Kh, dK = scale*dS^T.Qh; GQA: dK, dV of a KV head sum over
  * the query heads that read it.  BF16 tensor-core MMAs (P and dS rounded to BF16), fp32
- * accumulation, BF16 outputs.  Uses no memory beyond its arguments.
+ * accumulation, BF16 outputs.  Uses no memory beyond its arguments and the caller's workspace.
  */
 bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream);
+
+/*
+ * Bytes of workspace bf16_attn_bwd needs: 2 * 4 * B * Hq * (128 * ceil(S / 128)); 0 if a size is
+ * not positive.  Host only, no CUDA call.
+ */
+size_t bf16_attn_bwd_workspace_bytes(int B, int S, int Hq);
 
 /*
  * Synchronises `stream`, reads the int32 at `dev_status` and returns BSC_OK (0) or
