@@ -293,7 +293,7 @@ class Workload1:
         g = torch.Generator(device="cpu").manual_seed(3)
         d_o = torch.randn(self.q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(self.dev)
         dq, dk, dv = (torch.empty(t.shape, dtype=torch.bfloat16, device=self.dev) for t in (self.q, self.k, self.k))
-        ws = torch.empty(ops.bf16_attn_bwd_workspace_bytes(w.B, w.S, w.Hq), dtype=torch.uint8, device=self.dev)
+        ws = torch.empty(ops.bf16_attn_bwd_workspace_bytes(w.B, w.S, w.Hq, w.Hkv), dtype=torch.uint8, device=self.dev)
         self.step(p_terms, torch.cuda.Event(enable_timing=True))
         qq, qs, kq, ks, _, _, vtn, vtn_sc = self.quant
         call = lambda: ops.bf16_attn_bwd(qq, qs, kq, ks, vtn, vtn_sc, self.o, self.lse, d_o, w.layout, w.scale,

@@ -44,7 +44,7 @@ def _load():
     lib.bf16_attn_bwd.restype = i32
     lib.bf16_attn_bwd.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
     lib.bf16_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.bf16_attn_bwd_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.bf16_attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.bsc_read_device_status.restype = i32
     lib.bsc_read_device_status.argtypes = [vp, vp]
     return lib
@@ -255,16 +255,16 @@ def forward(q, k, v, layout=BSHD, softmax_scale=None, p_terms=2, leaky=0, o=None
                                  o=o, lse=lse, stream=stream, o8_out=o8_out, bf16_out=bf16_out)
 
 
-def bf16_attn_bwd_workspace_bytes(B, S, Hq):
+def bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv):
     """Bytes of scratch the backward needs (the C call of the same name)."""
-    return int(lib.bf16_attn_bwd_workspace_bytes(B, S, Hq))
+    return int(lib.bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv))
 
 
 def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softmax_scale=None, dq=None, dk=None,
                   dv=None, dev_status=None, wait_timeout_ms=0, stream=None, workspace=None):
     """Backward on decoded operands (quantised Q, K and token-normalised V, the forward's O, LSE);
     returns (dQ, dK, dV) in bf16, laid out like q and k.  `workspace`: a device tensor of at least
-    bf16_attn_bwd_workspace_bytes(B, S, Hq) bytes, else one is allocated here."""
+    bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv) bytes, else one is allocated here."""
     B, S, Hq, D = _bshd_dims(q, layout)
     Hkv = _bshd_dims(k, layout)[2]
     if softmax_scale is None:
@@ -274,7 +274,7 @@ def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softma
     dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dk is None else dk
     dv = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dv is None else dv
-    ws_bytes = bf16_attn_bwd_workspace_bytes(B, S, Hq)
+    ws_bytes = bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     p = AttnBwdParams(q=q.data_ptr(), q_sc=q_sc.data_ptr(), k=k.data_ptr(), k_sc=k_sc.data_ptr(),

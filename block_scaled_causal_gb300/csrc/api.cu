@@ -97,6 +97,20 @@ bool encode_bf16_tokens_map(CUtensorMap* m, const void* base, int B, int S, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 planes [planes][rows][128] (the backward's workspace) as a 3-D map with a 64-element x
+// 128-row box and the 128-byte swizzle: two boxes cover a tile's 128 columns.
+bool encode_bf16_planar_map(CUtensorMap* m, void* base, long long planes, int rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {256, (cuuint64_t)rows * 256};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Transposed V bytes [rows = B*H*D][S] as a 2-D map with a 128-key x 128-row box.
 bool encode_vt_map(CUtensorMap* m, const void* base, long long rows, int S) {
   auto enc = get_encode();
@@ -299,9 +313,9 @@ bsc_status mxfp8_causal_attn_fwd(const bsc_attn_fwd_params* p, bsc_stream_t stre
   return from_cuda(bsc::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t bf16_attn_bwd_workspace_bytes(int B, int S, int Hq) {
-  if (B <= 0 || S <= 0 || Hq <= 0) return 0;
-  return (size_t)2 * sizeof(float) * (size_t)B * (size_t)Hq * (size_t)((S + 127) / 128 * 128);
+size_t bf16_attn_bwd_workspace_bytes(int B, int S, int Hq, int Hkv) {
+  if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0) return 0;
+  return bsc::bwd_workspace_bytes(B, S, Hq, Hkv);
 }
 
 bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
@@ -321,17 +335,26 @@ bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
                         p->lse, p->d_o, p->dq, p->dk,   p->dv, p->workspace, p->dev_status};
   for (const void* q : ptrs)
     if (!aligned16(q)) return BSC_ERR_ALIGN;
-  if (p->workspace_bytes < bf16_attn_bwd_workspace_bytes(p->B, p->S, p->Hq)) return BSC_ERR_SHAPE;
+  if (p->workspace_bytes < bf16_attn_bwd_workspace_bytes(p->B, p->S, p->Hq, p->Hkv)) return BSC_ERR_SHAPE;
   if ((s = check_device()) != BSC_OK) return s;
 
   bsc::BwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!encode_tokens_map(&a.tm_q, p->q, p->B, p->S, p->Hq, p->layout, true) ||
-      !encode_tokens_map(&a.tm_k, p->k, p->B, p->S, p->Hkv, p->layout, true) ||
-      !encode_tokens_map(&a.tm_vtn, p->vtn, p->B, p->S, p->Hkv, p->layout, false) ||
-      !encode_bf16_tokens_map(&a.tm_do, p->d_o, p->B, p->S, p->Hq, p->layout) ||
-      !encode_bf16_tokens_map(&a.tm_o, p->o, p->B, p->S, p->Hq, p->layout))
+  const int Sp = (p->S + 127) / 128 * 128;
+  const long long rq = (long long)p->B * p->Hq * Sp, rk = (long long)p->B * p->Hkv * Sp;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(p->workspace);
+  a.ws = p->workspace;
+  a.qh = reinterpret_cast<uint16_t*>(ws + 8 * rq);
+  a.kh = a.qh + rq * 128;
+  a.vh = a.kh + rk * 128;
+  if (!encode_bf16_planar_map(&a.tm_qh, a.qh, (long long)p->B * p->Hq, Sp) ||
+      !encode_bf16_planar_map(&a.tm_kh, a.kh, (long long)p->B * p->Hkv, Sp) ||
+      !encode_bf16_planar_map(&a.tm_vh, a.vh, (long long)p->B * p->Hkv, Sp) ||
+      !encode_bf16_tokens_map(&a.tm_do, p->d_o, p->B, p->S, p->Hq, p->layout))
     return BSC_ERR_CUDA;
+  a.q8 = p->q;
+  a.k8 = p->k;
+  a.vtn = p->vtn;
   a.q_sc = p->q_sc;
   a.k_sc = p->k_sc;
   a.vtn_sc = p->vtn_sc;
@@ -341,8 +364,7 @@ bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream) {
   a.dq = p->dq;
   a.dk = p->dk;
   a.dv = p->dv;
-  a.ws = p->workspace;
-  a.Sp = (p->S + 127) / 128 * 128;
+  a.Sp = Sp;
   a.dev_status = p->dev_status;
   a.limit_ns = (unsigned long long)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
   a.B = p->B;

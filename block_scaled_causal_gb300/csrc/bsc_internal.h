@@ -54,16 +54,18 @@ struct AttnArgs {
 
 cudaError_t launch_attn_fwd(const AttnArgs& args, cudaStream_t st);
 
-// Arguments of the backward kernels (dQ, and dK/dV).
+// Arguments of the backward kernels (prep, dQ, and dK/dV).
 struct BwdArgs {
-  CUtensorMap tm_q;     // Q bytes, as in AttnArgs
-  CUtensorMap tm_k;     // K bytes, as in AttnArgs
-  CUtensorMap tm_vtn;   // token-normalised V bytes, as in AttnArgs
+  CUtensorMap tm_qh;    // decoded Q, BF16 workspace planes [B*Hq][Sp][D], box {64,128,1}, 128-byte swizzle
+  CUtensorMap tm_kh;    // decoded K, [B*Hkv][Sp][D], likewise
+  CUtensorMap tm_vh;    // decoded token-normalised V, [B*Hkv][Sp][D], likewise
   CUtensorMap tm_do;    // dO bf16, 4-D {D, Hq, S, B}, box {64,1,128,1}, 128-byte swizzle
-  CUtensorMap tm_o;     // O bf16, same form as dO
+  const uint8_t* q8;    // Q bytes, `layout`, Hq heads
+  const uint8_t* k8;    // K bytes, `layout`, Hkv heads
+  const uint8_t* vtn;   // token-normalised V bytes, `layout`, Hkv heads
   const uint8_t* q_sc;  // compact [B][Hq][S][4]
   const uint8_t* k_sc;  // compact [B][Hkv][S][4]
-  const uint8_t* vtn_sc;
+  const uint8_t* vtn_sc;  // [B][Hkv][S]
   const void* o;        // bf16 O of the forward, Q's layout
   const void* dO;       // bf16 dO, Q's layout
   const float* lse;     // [B][Hq][S], natural log
@@ -71,12 +73,19 @@ struct BwdArgs {
   void* dk;             // bf16, K's layout
   void* dv;             // bf16, K's layout
   float* ws;            // workspace: Dlt [B][Hq][Sp], then LSE * log2(e) [B][Hq][Sp]
+  uint16_t* qh;         // workspace: the BF16 planes behind tm_qh, tm_kh, tm_vh
+  uint16_t* kh;
+  uint16_t* vh;
   int32_t* dev_status;
   unsigned long long limit_ns;
   int B, S, Hq, Hkv, layout;
   int Sp;               // S rounded up to the 128-row tile
   float scale, scale_log2e;
 };
+
+// Workspace bytes of the backward: the statistics (2 x 4 B per query row) and the BF16 planes of
+// Qh, Kh and Vt (256 B per row), rows padded to Sp.
+size_t bwd_workspace_bytes(int B, int S, int Hq, int Hkv);
 
 cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st);
 

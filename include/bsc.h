@@ -237,10 +237,11 @@ typedef struct {
   float softmax_scale;    /* finite and > 0, else BSC_ERR_UNSUPPORTED */
   int32_t* dev_status;    /* optional, as in bsc_attn_fwd_params */
   uint32_t wait_timeout_ms;
-  /* [scratch] device memory of at least bf16_attn_bwd_workspace_bytes(B, S, Hq) bytes, 16-byte
-   * aligned, overlapping no other argument; owned by the caller, contents on entry ignored,
-   * on return undefined.  The call writes the per-row statistics of the backward there (Dlt_i and
-   * LSE_i*log2(e), fp32, rows padded to a multiple of 128) once, for both backward kernels.
+  /* [scratch] device memory of at least bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv) bytes,
+   * 16-byte aligned, overlapping no other argument; owned by the caller, contents on entry
+   * ignored, on return undefined.  The call first writes there, once, what both backward kernels
+   * read: Qh, Kh and the token-normalised Vt decoded to BF16 (one plane per batch and head, rows
+   * padded to a multiple of 128 with zeros) and the per-row statistics Dlt_i and LSE_i*log2(e).
    * NULL: BSC_ERR_NULL; workspace_bytes below the required size: BSC_ERR_SHAPE. */
   float* workspace;
   size_t workspace_bytes;
@@ -259,10 +260,11 @@ typedef struct {
 bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream);
 
 /*
- * Bytes of workspace bf16_attn_bwd needs: 2 * 4 * B * Hq * (128 * ceil(S / 128)); 0 if a size is
- * not positive.  Host only, no CUDA call.
+ * Bytes of workspace bf16_attn_bwd needs: B * Sp * (8 * Hq + 256 * (Hq + 2 * Hkv)) with
+ * Sp = 128 * ceil(S / 128) (fp32 statistics per query row, a BF16 row of D = 128 per query and
+ * per key and value row); 0 if a size is not positive.  Host only, no CUDA call.
  */
-size_t bf16_attn_bwd_workspace_bytes(int B, int S, int Hq);
+size_t bf16_attn_bwd_workspace_bytes(int B, int S, int Hq, int Hkv);
 
 /*
  * Synchronises `stream`, reads the int32 at `dev_status` and returns BSC_OK (0) or

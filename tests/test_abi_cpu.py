@@ -109,22 +109,25 @@ def test_attn_validation(ops, kw, want):
 def test_bwd_validation(ops):
     base = dict(q=FAKE, q_sc=FAKE, k=FAKE, k_sc=FAKE, vtn=FAKE, vtn_sc=FAKE, o=FAKE, lse=FAKE, d_o=FAKE, dq=FAKE,
                 dk=FAKE, dv=FAKE, B=1, S=256, Hq=4, Hkv=2, D=128, layout=0, softmax_scale=0.088, dev_status=0,
-                wait_timeout_ms=0, workspace=FAKE, workspace_bytes=1 << 20)
+                wait_timeout_ms=0, workspace=FAKE, workspace_bytes=1 << 30)
     for kw, want in ((dict(softmax_scale=-1.0), 4), (dict(softmax_scale=float("nan")), 4), (dict(Hq=3), 2),
                      (dict(dq=0), 1), (dict(dk=FAKE + 8), 3), (dict(S=0), 0), (dict(workspace=0), 1),
-                     (dict(workspace=FAKE + 4), 3), (dict(workspace_bytes=8192 - 4), 2)):
+                     (dict(workspace=FAKE + 4), 3), (dict(workspace_bytes=256 * (8 * 4 + 256 * 8) - 1), 2)):
         p = ops.AttnBwdParams(**dict(base, **kw))
         assert ops.lib.bf16_attn_bwd(ctypes.byref(p), None) == want, kw
     assert ops.lib.bf16_attn_bwd(None, None) == 1
 
 
 def test_bwd_workspace_bytes(ops):
-    # two fp32 planes [B][Hq][128 * ceil(S / 128)]
-    assert ops.bf16_attn_bwd_workspace_bytes(1, 256, 4) == 2 * 4 * 4 * 256
-    assert ops.bf16_attn_bwd_workspace_bytes(2, 160, 3) == 2 * 4 * 2 * 3 * 256
-    assert ops.bf16_attn_bwd_workspace_bytes(1, 32768, 16) == 2 * 4 * 16 * 32768
-    assert ops.bf16_attn_bwd_workspace_bytes(0, 256, 4) == 0
-    assert ops.bf16_attn_bwd_workspace_bytes(1, 0, 4) == 0
+    # per padded row: fp32 Dlt and LSE per query row, a 128-element BF16 row per query, key, value
+    def want(B, S, Hq, Hkv):
+        Sp = -(-S // 128) * 128
+        return B * Sp * (8 * Hq + 256 * (Hq + 2 * Hkv))
+    for args in ((1, 256, 4, 2), (2, 160, 3, 1), (1, 32768, 16, 4), (2, 32768, 16, 16)):
+        assert ops.bf16_attn_bwd_workspace_bytes(*args) == want(*args), args
+    assert ops.bf16_attn_bwd_workspace_bytes(0, 256, 4, 2) == 0
+    assert ops.bf16_attn_bwd_workspace_bytes(1, 0, 4, 2) == 0
+    assert ops.bf16_attn_bwd_workspace_bytes(1, 256, 4, 0) == 0
 
 
 def test_attn_null_params(ops):
