@@ -79,59 +79,59 @@ __device__ __forceinline__ uint2 decode4_bf16(uint32_t x, uint32_t scale2) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// prep.  One warp per row of one of four jobs, in this order of the row index:
-//   Qh rows (B*Hq*Sp), Kh rows (B*Hkv*Sp), Vt rows (B*Hkv*Sp): 128 E4M3 bytes -> 128 BF16 (lane l
-//     takes bytes 4l..4l+3, whose scale is the row's block l/8: Q and K rowwise scales, or V's
-//     one amplitude per token);
-//   statistics rows (B*Hq*Sp): Dlt_i = <dO_i, O_i> (fp32) and LSE_i log2(e).
+// prep.  Grid (Sp / 64, B * Hq, 4): block z picks the job, y the (batch, head) plane, x a run of
+// 64 rows; each of the 8 warps takes 8 rows.
+//   z = 0, 1, 2: Qh, Kh, Vt rows: 128 E4M3 bytes -> 128 BF16 (lane l takes bytes 4l..4l+3, whose
+//     scale is the row's block l / 8: Q and K rowwise scales, or V's one amplitude per token);
+//     planes past B * Hkv are idle for Kh and Vt;
+//   z = 3: statistics: Dlt_i = <dO_i, O_i> (fp32) and LSE_i log2(e).
 // Rows at or past S: zero BF16 rows, Dlt = 0 and LSE = +inf, which make their P and dS exactly 0.
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ BwdArgs a) {
-  const int lane = threadIdx.x & 31;
-  const long long rq = (long long)a.B * a.Hq * a.Sp, rk = (long long)a.B * a.Hkv * a.Sp;
-  long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r < rq + 2 * rk) {
-    const bool is_q = r < rq, is_k = !is_q && r < rq + rk;
-    if (!is_q) r -= is_k ? rq : rq + rk;
-    const int H = is_q ? a.Hq : a.Hkv;
-    const int i = (int)(r % a.Sp);
-    const long long bh = r / a.Sp;
-    const int h = (int)(bh % H), b = (int)(bh / H);
-    uint2 out = make_uint2(0u, 0u);
-    if (i < a.S) {
-      const long long row = a.layout == 0 ? ((long long)b * a.S + i) * H + h : ((long long)i * a.B + b) * H + h;
-      const uint8_t* src = is_q ? a.q8 : is_k ? a.k8 : a.vtn;
-      const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(src + row * HD) + lane);
-      const uint32_t sb = is_q ? __ldg(a.q_sc + (bh * a.S + i) * 4 + (lane >> 3))
-                          : is_k ? __ldg(a.k_sc + (bh * a.S + i) * 4 + (lane >> 3))
-                                 : __ldg(a.vtn_sc + bh * a.S + i);
-      out = decode4_bf16(x, bf16x2_pow2_e8m0(sb));
+  const int lane = threadIdx.x & 31, job = blockIdx.z;
+  const int plane = blockIdx.y;   // b * H + h
+  const int H = job == 0 || job == 3 ? a.Hq : a.Hkv;
+  if (plane >= a.B * H) return;
+  const int b = plane / H, h = plane - b * H;
+  const int i0 = blockIdx.x * 64 + (threadIdx.x >> 5) * 8;
+  const long long prow = (long long)plane * a.Sp;   // the plane's first row in the workspace
+  if (job < 3) {
+    const uint8_t* src = job == 0 ? a.q8 : job == 1 ? a.k8 : a.vtn;
+    uint16_t* dst = job == 0 ? a.qh : job == 1 ? a.kh : a.vh;
+#pragma unroll 2
+    for (int i = i0; i < i0 + 8; ++i) {
+      uint2 out = make_uint2(0u, 0u);
+      if (i < a.S) {
+        const long long row = a.layout == 0 ? ((long long)b * a.S + i) * H + h : ((long long)i * a.B + b) * H + h;
+        const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(src + row * HD) + lane);
+        const uint32_t sb = job == 2 ? __ldg(a.vtn_sc + (long long)plane * a.S + i)
+                                     : __ldg((job == 0 ? a.q_sc : a.k_sc) + ((long long)plane * a.S + i) * 4 + (lane >> 3));
+        out = decode4_bf16(x, bf16x2_pow2_e8m0(sb));
+      }
+      reinterpret_cast<uint2*>(dst + (prow + i) * HD)[lane] = out;
     }
-    uint16_t* dst = is_q ? a.qh : is_k ? a.kh : a.vh;
-    reinterpret_cast<uint2*>(dst + r * HD)[lane] = out;
     return;
   }
-  r -= rq + 2 * rk;
-  if (r >= rq) return;
-  const int i = (int)(r % a.Sp);
-  const long long bh = r / a.Sp;
-  const int hq = (int)(bh % a.Hq), b = (int)(bh / a.Hq);
-  float acc = 0.f;
-  if (i < a.S) {
-    const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + hq : ((long long)i * a.B + b) * a.Hq + hq;
-    const uint2 x = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + row * HD) + lane);
-    const uint2 y = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + row * HD) + lane);
-    const uint32_t xs[2] = {x.x, x.y}, ys[2] = {y.x, y.y};
+  const long long plane_rows = (long long)a.B * a.Hq * a.Sp;
+#pragma unroll 2
+  for (int i = i0; i < i0 + 8; ++i) {
+    float acc = 0.f;
+    if (i < a.S) {
+      const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + h : ((long long)i * a.B + b) * a.Hq + h;
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + row * HD) + lane);
+      const uint2 y = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + row * HD) + lane);
+      const uint32_t xs[2] = {x.x, x.y}, ys[2] = {y.x, y.y};
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
-      acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+      for (int e = 0; e < 2; ++e) {
+        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+      }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  if (lane == 0) {
-    a.ws[r] = i < a.S ? acc : 0.f;
-    a.ws[rq + r] = i < a.S ? a.lse[bh * a.S + i] * 1.4426950408889634f : INFINITY;
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) {
+      a.ws[prow + i] = i < a.S ? acc : 0.f;
+      a.ws[plane_rows + prow + i] = i < a.S ? a.lse[(long long)plane * a.S + i] * 1.4426950408889634f : INFINITY;
+    }
   }
 }
 
@@ -482,31 +482,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 //   S   = Qh Kh_j^T     (B = Kh [key][d], K-major)
 //   dP  = dO Vt_j^T     (B = Vt [key][d], K-major)
 //   P   = exp2(S scale log2(e) - LSE2),  dS = P (dP - Dlt)     (softmax warps, one query row each)
-//   dQ += dS Kh_j       A = dS (BF16 over the first 64 columns of dP), B = Kh read along the keys
+//   dQ += dS Kh_j       A = dS (BF16 over dP's columns 0-31 and 64-95), B = Kh read along the keys
 // Issue order S(0) dP(0) | S(j+1) dQ(j) dP(j+1) | ...: S(j+1) follows as soon as the softmax warps
 // have read S(j) (P stays in registers), so P(j+1) runs under dQ(j) and dP(j+1), and dS(j+1) under
 // S(j+2).  dP(j+1) rewrites the columns dQ(j) reads and is issued after it.
 // TMEM: Qh 0-63, dO 64-127, S 128-255, dP 256-383, dQ 384-511.
-constexpr uint32_t QQ_QH = 0;            // Qh bf16 [q][d], copied into TMEM at the start
-constexpr uint32_t QQ_DO = TILE;         // dO bf16 [q][d], likewise
-constexpr uint32_t QQ_KH = 2 * TILE;     // 2 stages: Kh bf16 [key][d]
-constexpr uint32_t QQ_VH = 4 * TILE;     // 2 stages: Vt bf16 [key][d]
-constexpr uint32_t QQ_STAT = 6 * TILE;   // Dlt[128], then LSE2[128]
+// Key tiles go round three shared-memory stages of 64 KB (Kh, then Vt); Qh and dO arrive in stage
+// 2, which takes its first key tile (tile 2) once they have been copied into TMEM.
+constexpr int KST = 3;                      // key-tile stages
+constexpr uint32_t QQ_STAGE = 2 * TILE;     // stage s at s * QQ_STAGE: Kh bf16 [key][d], then Vt
+constexpr uint32_t QQ_QH = 2 * QQ_STAGE;    // Qh bf16 [q][d], then dO: in stage 2 at the start
+constexpr uint32_t QQ_DO = QQ_QH + TILE;
+constexpr uint32_t QQ_STAT = KST * QQ_STAGE;   // Dlt[128], then LSE2[128]
 constexpr uint32_t QQ_BAR = QQ_STAT + 1024;
 constexpr uint32_t QQ_MISC = QQ_BAR + 128;   // TMEM slot, abort flag
 constexpr uint32_t QQ_SMEM = QQ_MISC + 16 + 1024;
 static_assert(QQ_SMEM <= 227 * 1024, "shared memory budget");
 constexpr uint32_t T_QH = 0, T_DOH = 64, T_S = 128, T_DP = 256, T_DQ = 384;
-// mbarriers: QD (Qh, dO and the statistics of the tile), KF + st (a key tile's Kh and Vt in stage
-// st), SF (S(j) computed), DP (dP(j) computed), KD + st (the MMAs of the key tile in stage st have
-// completed, up to dQ(j)).
-enum QBar : uint32_t { QB_QD = 0, QB_KF = 1, QB_SF = 3, QB_DP, QB_KD, QB_DRAIN = QB_KD + 2, QB_COUNT };
+// mbarriers: QD (Qh, dO and the statistics of the tile), CP (Qh and dO copied into TMEM), KF + s (a
+// key tile's Kh and Vt landed in stage s), SF (S(j) computed), DP (dP(j) computed), KD + s (the
+// MMAs of the key tile in stage s have completed, up to dQ(j)).
+enum QBar : uint32_t {
+  QB_QD = 0, QB_CP, QB_KF, QB_SF = QB_KF + KST, QB_DP, QB_KD, QB_DRAIN = QB_KD + KST, QB_COUNT
+};
 static_assert(QB_COUNT * 8 <= 128, "barrier slots");
-// Named barriers, softmax warps (128) + MMA warp (32), with the rules of the dK/dV kernel:
+// Named barriers, softmax warps (256) + MMA warp (32), with the rules of the dK/dV kernel:
 //   NB_LD  a key tile landed;  NB_S  S(j) has been read;  NB_DS  dS(j) is in TMEM (blocking).
+// 12 warps: the softmax work of a query row is split between two warps of the same TMEM lane
+// quarter (warps 4-7 keys 0-63, warps 8-11 keys 64-127); each writes its dS over its own dP
+// columns (keys 64 kh.. at columns 64 kh..64 kh+31), the A operand of dQ in two K halves.
+constexpr int kThreadsDq = 384;
+constexpr uint32_t kNbDq = 256 + 32;
 constexpr uint32_t NB_S = 2;
 
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -552,13 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       prefetch_tensormap(&a.tm_vh);
       prefetch_tensormap(&a.tm_do);
       auto load_kv = [&](int j) {
-        const uint32_t fb = bar(QB_KF + (j & 1));
+        const int st = j % KST;
+        const uint32_t fb = bar(QB_KF + st);
         mbar_arrive_expect_tx(fb, 2 * TILE);
-        load_plane_tile(sbase + QQ_KH + (j & 1) * TILE, &a.tm_kh, fb, j * BN, kv_plane);
-        load_plane_tile(sbase + QQ_VH + (j & 1) * TILE, &a.tm_vh, fb, j * BN, kv_plane);
+        load_plane_tile(sbase + st * QQ_STAGE, &a.tm_kh, fb, j * BN, kv_plane);
+        load_plane_tile(sbase + st * QQ_STAGE + TILE, &a.tm_vh, fb, j * BN, kv_plane);
       };
       bool ok = start_ok;
-      int nl[2] = {0, 0};
+      int nl[KST] = {0, 0, 0};
       if (ok) {
         const long long srow = q_plane * a.Sp + (long long)it * BM;
         mbar_arrive_expect_tx(bar(QB_QD), 2 * TILE + 1024);
@@ -570,15 +580,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
           load_kv(j);
           nl[j] = 1;
         }
+        // stage 2 once Qh and dO have been copied out of it
+        if (J > 2 && (ok = mbar_wait(bar(QB_CP), 0, ctl, W_PROD))) {
+          load_kv(2);
+          nl[2] = 1;
+        }
       }
-      // stage j % 2 takes key tile j + 2 once the MMAs of tile j (its last readers) have completed
-      for (int j = 0; ok && j + 2 < J; ++j) {
-        if (!(ok = mbar_wait(bar(QB_KD + (j & 1)), (uint32_t)(j >> 1) & 1u, ctl, W_PROD))) break;
-        load_kv(j + 2);
-        ++nl[j & 1];
+      // stage j % 3 takes key tile j + 3 once the MMAs of tile j (its last readers) have completed
+      for (int j = 0; ok && j + KST < J; ++j) {
+        if (!(ok = mbar_wait(bar(QB_KD + j % KST), (uint32_t)(j / KST) & 1u, ctl, W_PROD))) break;
+        load_kv(j + KST);
+        ++nl[j % KST];
       }
       if (start_ok) mbar_wait_drain(bar(QB_QD), 0, a.limit_ns);
-      for (int st = 0; st < 2; ++st)
+      for (int st = 0; st < KST; ++st)
         if (nl[st] > 0) mbar_wait_drain(bar(QB_KF + st), (uint32_t)(nl[st] - 1) & 1u, a.limit_ns);
     }
     __syncwarp();
@@ -591,14 +606,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         tc_fence_after();
         tile_to_tmem(tmem + T_QH, sbase + QQ_QH);
         tile_to_tmem(tmem + T_DOH, sbase + QQ_DO);
+        tc_commit(bar(QB_CP));
       }
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
     auto live = [&]() { return ok && *abort_flag == 0; };
-    const uint64_t dKk = desc_kmajor_sw128(sbase + QQ_KH), dVk = desc_kmajor_sw128(sbase + QQ_VH);
-    const uint64_t dKm = smem_desc(sbase + QQ_KH, ATOM, 1024, 2);
+    const uint64_t dKk = desc_kmajor_sw128(sbase), dVk = desc_kmajor_sw128(sbase + TILE);
+    const uint64_t dKm = smem_desc(sbase, ATOM, 1024, 2);
     constexpr uint32_t idN = idesc_bf16(BM, BN), idMN = idesc_bf16(BM, HD) | (1u << 16);
-    auto soff = [](int j) { return (uint32_t)(((j & 1) * TILE) >> 4); };
+    auto soff = [](int j) { return (uint32_t)(((j % KST) * QQ_STAGE) >> 4); };
     auto issue_s = [&](int j) {
       mma_ts<8, false>(tmem + T_S, tmem + T_QH, dKk + soff(j), idN, 0u);
       tc_commit(bar(QB_SF));
@@ -607,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       mma_ts<8, false>(tmem + T_DP, tmem + T_DOH, dVk + soff(j), idN, 0u);
       tc_commit(bar(QB_DP));
     };
-    named_sync(NB_LD, kNb);
+    named_sync(NB_LD, kNbDq);
     if (lane == 0 && live()) {
       tc_fence_after();
       issue_s(0);
@@ -615,20 +631,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     }
     __syncwarp();
     for (int j = 0; j < J; ++j) {
-      named_sync(NB_S, kNb);
+      named_sync(NB_S, kNbDq);
       if (j + 1 < J) {
-        named_sync(NB_LD, kNb);
+        named_sync(NB_LD, kNbDq);
         if (lane == 0 && live()) {
           tc_fence_after();
           issue_s(j + 1);
         }
         __syncwarp();
       }
-      named_sync(NB_DS, kNb);
+      named_sync(NB_DS, kNbDq);
       if (lane == 0 && live()) {   // dQ += dS Kh
         tc_fence_after();
-        mma_ts<8, true>(tmem + T_DQ, tmem + T_DP, dKm + soff(j), idMN, j > 0 ? 1u : 0u);
-        tc_commit(bar(QB_KD + (j & 1)));
+        mma_ts<4, true>(tmem + T_DQ, tmem + T_DP, dKm + soff(j), idMN, j > 0 ? 1u : 0u);
+        mma_ts<4, true>(tmem + T_DQ, tmem + T_DP + 64, dKm + soff(j) + 4 * (2048 >> 4), idMN, 1u);
+        tc_commit(bar(QB_KD + j % KST));
         if (j + 1 < J) issue_dp(j + 1);
       }
       __syncwarp();
@@ -636,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     if (lane == 0) tc_commit(bar(QB_DRAIN));
     __syncwarp();
   } else if (warp >= 4) {
-    // ======================= softmax: query row r of the tile per thread
-    const int qq = warp & 3, r = qq * 32 + lane;
+    // ======================= softmax: query row r of the tile per thread, keys 64 kh.. of it
+    const int qq = warp & 3, r = qq * 32 + lane, kh = (warp - 4) >> 2;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     const float sl2 = a.scale_log2e;
     bool ok = start_ok;
@@ -647,48 +664,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     // key tile j landed; then its generation of NB_LD.  The first is met blocking: the arrival for
     // tile 1 then follows the MMA warp's passing of tile 0's generation also when a wait failed.
     auto landed = [&](int j) {
-      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(QB_KF + (j & 1)), (uint32_t)(j >> 1) & 1u, ctl, W_SM_LD));
-      if (j == 0) named_sync(NB_LD, kNb);
-      else named_arrive(NB_LD, kNb);
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(QB_KF + j % KST), (uint32_t)(j / KST) & 1u, ctl, W_SM_LD));
+      if (j == 0) named_sync(NB_LD, kNbDq);
+      else named_arrive(NB_LD, kNbDq);
     };
     auto tile = [&](int j, auto diag_tag) {
       constexpr bool DIAG = decltype(diag_tag)::value;
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(QB_SF), (uint32_t)j & 1u, ctl, W_SM_S));
-      float p[128];
+      float p[64];
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tld32(tmem + lane_off + T_S + 32 * c, p + 32 * c);
+        for (int c = 0; c < 2; ++c) tld32(tmem + lane_off + T_S + 64 * kh + 32 * c, p + 32 * c);
         tmem_ld_wait();
         tc_fence_before();
       }
-      named_arrive(NB_S, kNb);   // S(j) is in registers: S(j+1) may be computed over it
+      named_arrive(NB_S, kNbDq);   // S(j) is in registers: S(j+1) may be computed over it
+      if (j + 1 < J) landed(j + 1);   // and, once its tile landed, issued right away
       if (ok) {
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
+        for (int k = 0; k < 64; ++k) {
           const float x = ex2_approx(fmaf(p[k], sl2, -lse2));
-          p[k] = (DIAG && k > r) ? 0.f : x;   // in the diagonal tile a query sees keys up to itself
+          p[k] = (DIAG && 64 * kh + k > r) ? 0.f : x;   // in the diagonal tile a query sees keys up to itself
         }
       }
-      if (j + 1 < J) landed(j + 1);
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(QB_DP), (uint32_t)j & 1u, ctl, W_SM_DP));
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {   // dS of keys 32c.. over columns 16c.., read by then
+        for (int c = 0; c < 2; ++c) {   // dS of keys 64 kh + 32c.. over columns 64 kh + 16c.., read by then
           float d[32];
           uint32_t w[16];
-          tld32(tmem + lane_off + T_DP + 32 * c, d);
+          tld32(tmem + lane_off + T_DP + 64 * kh + 32 * c, d);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[i] = pack_bf16x2(p[32 * c + 2 * i] * (d[2 * i] - dlt), p[32 * c + 2 * i + 1] * (d[2 * i + 1] - dlt));
-          tst16(tmem + lane_off + T_DP + 16 * c, w);
+          tst16(tmem + lane_off + T_DP + 64 * kh + 16 * c, w);
         }
         tmem_st_wait();
         tc_fence_before();
       }
-      named_sync(NB_DS, kNb);
+      named_sync(NB_DS, kNbDq);
     };
     landed(0);
     for (int j = 0; j < J - 1; ++j) tile(j, std::false_type{});
@@ -700,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   __syncthreads();
   const bool drained = mbar_wait_drain(bar(QB_DRAIN), 0, a.limit_ns);
   tc_fence_after();
-  if (cta_all(drained && start_ok && *abort_flag == 0)) store_acc(tmem + T_DQ, a.dq, a, a.Hq, b, hq, it, a.scale);
+  if (cta_all(drained && start_ok && *abort_flag == 0) && warp < 8) store_acc(tmem + T_DQ, a.dq, a, a.Hq, b, hq, it, a.scale);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -724,11 +741,11 @@ cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st) {
     attr_set = true;
   }
   const long long T = (args.S + BM - 1) / BM;
-  const long long rows = 2LL * args.B * args.Sp * (args.Hq + args.Hkv);
-  attn_bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(args);
+  if ((long long)args.B * args.Hq > 65535) return cudaErrorInvalidConfiguration;   // the prep grid's y
+  attn_bwd_prep_kernel<<<dim3((unsigned)(args.Sp / 64), (unsigned)(args.B * args.Hq), 4), 256, 0, st>>>(args);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_kernel<<<(unsigned)((long long)args.B * args.Hq * T), kThreads, QQ_SMEM, st>>>(args);
+  attn_bwd_dq_kernel<<<(unsigned)((long long)args.B * args.Hq * T), kThreadsDq, QQ_SMEM, st>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_bwd_dkdv_kernel<<<(unsigned)((long long)args.B * args.Hkv * T), kThreads, KV_SMEM, st>>>(args);
