@@ -40,7 +40,7 @@ FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 MAX_ABS, MEAN_ABS, LSE_REL = 3e-2, 3e-3, 1e-3
 # the large synthetic shapes timed in `configs` (the small one is a parity case only)
 BENCH_CONFIGS = ["gqa_s8k_h16_kv4", "mha_s16k_h16_heavy1pct", "gqa_s32k_h16_kv4", "mha_b2_s32k_h16_sbhd"]
-BWD_CONFIGS = {"mha_b2_s32k_h16_sbhd"}
+BWD_CONFIGS = {"gqa_s32k_h16_kv4", "mha_b2_s32k_h16_sbhd"}
 
 
 def max_over_ranks(x, world, device):
@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the backward on --workload (for profiling) and print one JSON line")
     return ap.parse_args()
 
 
@@ -356,6 +358,16 @@ def main():
     dev = torch.device("cuda", local)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)   # 256 MB > L2
     stream = torch.cuda.current_stream(dev)
+
+    if args.backward_only:   # the backward alone on --workload (the profile commands use this)
+        wb = Workload1(w, dev, ops, flush, stream)
+        bms = wb.backward_ms(args.p_terms, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"metric": "backward_ms", "value": bms, "unit": "ms", "higher_is_better": False,
+                              "config": {"workload": w.name}, "bwd_tflops": 2.5 * flops / (bms * 1e-3) / 1e12,
+                              "note": "backward on operands decoded from the MXFP8 bytes (prep, dQ and dK/dV "
+                                      "kernels), L2 flushed between calls"}), flush=True)
+        return
     hb = Workload1(w, dev, ops, flush, stream)
     q_cpu, k_cpu, v_cpu = hb.cpu
     q, k, v, o, lse = hb.q, hb.k, hb.v, hb.o, hb.lse
