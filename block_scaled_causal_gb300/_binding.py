@@ -43,6 +43,10 @@ def _load():
     lib.mxfp8_quantize.argtypes = [ctypes.POINTER(QuantParams), vp]
     lib.bf16_attn_bwd.restype = i32
     lib.bf16_attn_bwd.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
+    lib.bf16_attn_bwd_static.restype = i32
+    lib.bf16_attn_bwd_static.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
+    lib.bf16_attn_bwd_static_capacity.restype = ctypes.c_size_t
+    lib.bf16_attn_bwd_static_capacity.argtypes = []
     lib.bf16_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.bf16_attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.bsc_read_device_status.restype = i32
@@ -260,11 +264,8 @@ def bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv):
     return int(lib.bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv))
 
 
-def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softmax_scale=None, dq=None, dk=None,
-                  dv=None, dev_status=None, wait_timeout_ms=0, stream=None, workspace=None):
-    """Backward on decoded operands (quantised Q, K and token-normalised V, the forward's O, LSE);
-    returns (dQ, dK, dV) in bf16, laid out like q and k.  `workspace`: a device tensor of at least
-    bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv) bytes, else one is allocated here."""
+def _bwd_params(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout, softmax_scale, dq, dk, dv, dev_status,
+                wait_timeout_ms, workspace):
     B, S, Hq, D = _bshd_dims(q, layout)
     Hkv = _bshd_dims(k, layout)[2]
     if softmax_scale is None:
@@ -274,17 +275,43 @@ def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softma
     dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dk is None else dk
     dv = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dv is None else dv
-    ws_bytes = bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv)
-    if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     p = AttnBwdParams(q=q.data_ptr(), q_sc=q_sc.data_ptr(), k=k.data_ptr(), k_sc=k_sc.data_ptr(),
                       vtn=vtn.data_ptr(), vtn_sc=vtn_sc.data_ptr(), o=o.data_ptr(), lse=lse.data_ptr(),
                       d_o=do.data_ptr(), dq=dq.data_ptr(), dk=dk.data_ptr(), dv=dv.data_ptr(), B=B, S=S, Hq=Hq,
                       Hkv=Hkv, D=D, layout=layout, softmax_scale=softmax_scale,
                       dev_status=0 if dev_status is None else dev_status.data_ptr(), wait_timeout_ms=wait_timeout_ms,
-                      workspace=workspace.data_ptr(), workspace_bytes=workspace.numel() * workspace.element_size())
+                      workspace=0 if workspace is None else workspace.data_ptr(),
+                      workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+    return p, dq, dk, dv
+
+
+def bf16_attn_bwd(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softmax_scale=None, dq=None, dk=None,
+                  dv=None, dev_status=None, wait_timeout_ms=0, stream=None, workspace=None):
+    """Backward on decoded operands (quantised Q, K and token-normalised V, the forward's O, LSE);
+    returns (dQ, dK, dV) in bf16, laid out like q and k.  `workspace`: a device tensor of at least
+    bf16_attn_bwd_workspace_bytes(B, S, Hq, Hkv) bytes, else one is allocated here."""
+    if workspace is None:
+        B, S, Hq, _ = _bshd_dims(q, layout)
+        ws_bytes = bf16_attn_bwd_workspace_bytes(B, S, Hq, _bshd_dims(k, layout)[2])
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    p, dq, dk, dv = _bwd_params(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout, softmax_scale, dq, dk, dv,
+                                dev_status, wait_timeout_ms, workspace)
     _check(lib.bf16_attn_bwd(ctypes.byref(p), _stream(stream)))
     return dq, dk, dv
+
+
+def bf16_attn_bwd_static(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout=BSHD, softmax_scale=None, dq=None,
+                         dk=None, dv=None, dev_status=None, wait_timeout_ms=0, stream=None):
+    """bf16_attn_bwd with the library's fixed device workspace (nothing allocated for scratch)."""
+    p, dq, dk, dv = _bwd_params(q, q_sc, k, k_sc, vtn, vtn_sc, o, lse, do, layout, softmax_scale, dq, dk, dv,
+                                dev_status, wait_timeout_ms, None)
+    _check(lib.bf16_attn_bwd_static(ctypes.byref(p), _stream(stream)))
+    return dq, dk, dv
+
+
+def bf16_attn_bwd_static_capacity():
+    """Bytes of the fixed workspace bf16_attn_bwd_static uses."""
+    return int(lib.bf16_attn_bwd_static_capacity())
 
 
 def forward_backward(q, k, v, do, layout=BSHD, softmax_scale=None, p_terms=2, stream=None):

@@ -267,6 +267,20 @@ bsc_status bf16_attn_bwd(const bsc_attn_bwd_params* p, bsc_stream_t stream);
 size_t bf16_attn_bwd_workspace_bytes(int B, int S, int Hq, int Hkv);
 
 /*
+ * The backward of bf16_attn_bwd without caller scratch: `workspace` and `workspace_bytes` of *p are
+ * ignored and the call uses a fixed device array of this library (bf16_attn_bwd_static_capacity()
+ * bytes, taken when the library's module holding it is loaded), so it allocates nothing.  The
+ * pages have no counterpart of this call; it is a packaging of the same computation.  The array is
+ * shared by every call on a device: calls must not overlap in time (one stream, or synchronised).
+ * A call that needs more than the capacity: BSC_ERR_SHAPE, nothing launched.  Other arguments and
+ * errors as bf16_attn_bwd.
+ */
+bsc_status bf16_attn_bwd_static(const bsc_attn_bwd_params* p, bsc_stream_t stream);
+
+/* Bytes of the fixed workspace of bf16_attn_bwd_static.  Host only, no CUDA call. */
+size_t bf16_attn_bwd_static_capacity(void);
+
+/*
  * Synchronises `stream`, reads the int32 at `dev_status` and returns BSC_OK (0) or
  * BSC_ERR_DEVICE_TIMEOUT (non-zero).  The only call that synchronises.
  */
