@@ -205,21 +205,25 @@ __device__ __forceinline__ void ds_chunk(const float* p, const float* d, const f
 // ================================================================================================
 // dK, dV.  One CTA per (batch, KV head hk, 128-key tile jt); it walks the pairs n = 0..N-1 of (query
 // head of the group, query tile at or after jt): query tiles from the last down, the group's heads
-// innermost, so CTAs of one KV head running together read the same Qh and dO tiles from L2.  Each
-// pair's 128 queries are two sub-tiles of 64 (m = 2n + h), so that S^T and dP^T take 64 TMEM
-// columns each and Kh and Vt fit in tensor memory as the A operands:
-//   S^T  = Kh Qh_h^T    (M = 128 keys, N = 64 queries)
-//   dP^T = Vt dO_h^T
+// innermost, so CTAs of one KV head running together read the same Qh and dO tiles from L2.  The
+// keys sit on the TMEM lanes, so P^T and dS^T are the A operands of the dV and dK MMAs straight from
+// tensor memory:
+//   S^T  = Kh Qh^T      (M = 128 keys, N = 128 queries; A = Kh and B = Qh from shared memory)
+//   dP^T = Vt dO^T      (A = Vt, B = dO from shared memory)
 //   P^T  = exp2(S^T scale log2(e) - LSE2[q]),  dS^T = P^T (dP^T - Dlt[q])     (softmax warps)
-//   dV  += P^T dO_h     A = P^T (BF16 over the first 32 columns of S^T), B = dO read along q
-//   dK  += dS^T Qh_h    A = dS^T (BF16 over the first 32 columns of dP^T), B = Qh read along q
-// MMA issue order S(0) dP(0) | dV(m) S(m+1) dK(m) dP(m+1) | ...: the softmax of sub-tile m + 1 runs
-// under dK(m) and dP(m + 1), its dS under dV(m + 1) and S(m + 2).  An MMA that rewrites columns an
-// earlier one reads (S(m+1) over P^T(m), dP(m+1) over dS^T(m)) is issued after it: the MMAs of one
-// thread run in issue order.  TMEM: Kh 0-63, Vt 64-127, S^T 128-191, dP^T 192-255, dV 256-383,
+//   dV  += P^T dO       A = P^T (BF16 in S^T's columns), B = dO read along q
+//   dK  += dS^T Qh      A = dS^T (BF16 in dP^T's columns), B = Qh read along q
+// Kh and Vt stay in shared memory, so S^T and dP^T get 128 columns each (an MMA of N = 128 does
+// twice the work of one of N = 64 in about 1.25x the time).  Eight softmax warps: those of one TMEM
+// lane quarter take 64 queries each (warps 4-7 queries 0-63, warps 8-11 queries 64-127) and write
+// their BF16 P^T and dS^T over their own columns (queries 64 h.. at columns 64 h..64 h+31): the A
+// operands in two K halves.  MMA issue order S(0) dP(0) | dV(n) S(n+1) dK(n) dP(n+1) | ...: the
+// softmax of pair n + 1 runs under dK(n) and dP(n + 1), its dS under dV(n + 1) and S(n + 2).  An MMA
+// that rewrites columns an earlier one reads (S(n+1) over P^T(n), dP(n+1) over dS^T(n)) is issued
+// after it: the MMAs of one thread run in issue order.  TMEM: S^T 0-127, dP^T 128-255, dV 256-383,
 // dK 384-511.
-constexpr uint32_t KV_KH = 0;            // Kh bf16 [key][d], copied into TMEM at the start
-constexpr uint32_t KV_VH = TILE;         // Vt bf16 [key][d], likewise
+constexpr uint32_t KV_KH = 0;            // Kh bf16 [key][d]
+constexpr uint32_t KV_VH = TILE;         // Vt bf16 [key][d]
 constexpr uint32_t KV_QH = 2 * TILE;     // 2 stages: Qh bf16 [q][d]
 constexpr uint32_t KV_DO = 4 * TILE;     // 2 stages: dO bf16 [q][d]
 constexpr uint32_t KV_STAT = 6 * TILE;   // 2 stages: Dlt[128], then LSE2[128]
@@ -227,26 +231,27 @@ constexpr uint32_t KV_BAR = KV_STAT + 2048;
 constexpr uint32_t KV_MISC = KV_BAR + 128;   // TMEM slot, abort flag
 constexpr uint32_t KV_SMEM = KV_MISC + 16 + 1024;
 static_assert(KV_SMEM <= 227 * 1024, "shared memory budget");
-constexpr uint32_t T_KH = 0, T_VH = 64, T_ST = 128, T_DPT = 192, T_DV = 256, T_DK = 384;
+constexpr uint32_t T_ST = 0, T_DPT = 128, T_DV = 256, T_DK = 384;
+constexpr int kThreadsKv = 384;
 // mbarriers:
 //   KV        Kh and Vt landed
 //   LF + st   Qh, dO and the statistics of a pair landed in stage st
-//   SF        S^T(m) computed (and every MMA issued before it)
-//   DP        dP^T(m) computed
-//   PD + st   the MMAs of the pair in stage st have completed (up to dK of its second sub-tile)
+//   SF        S^T(n) computed (and every MMA issued before it)
+//   DP        dP^T(n) computed
+//   PD + st   the MMAs of the pair in stage st have completed (up to its dK)
 enum KvBar : uint32_t { KB_KV = 0, KB_LF = 1, KB_SF = 3, KB_DP, KB_PD, KB_DRAIN = KB_PD + 2, KB_COUNT };
 static_assert(KB_COUNT * 8 <= 128, "barrier slots");
-// Named barriers, softmax warps (128 threads) + MMA warp (32):
+// Named barriers, softmax warps (256 threads) + MMA warp (32):
 //   NB_LD   a pair's data landed (the softmax warps wait for the copies; once per pair)
-//   NB_P    P^T(m) is in TMEM
-//   NB_DS   dS^T(m) is in TMEM
+//   NB_P    P^T(n) is in TMEM
+//   NB_DS   dS^T(n) is in TMEM
 // The softmax warps block on NB_DS and arrive on the others: each blocking generation they pass
 // shows the MMA warp has passed the previous generation of every barrier they arrive on next, so no
-// generation ever holds arrivals of two sub-tiles, also once a role has given up (a failed wait:
-// it skips its work but meets every generation).  Both sides meet the generations in one order.
-constexpr uint32_t NB_LD = 1, NB_P = 2, NB_DS = 3, kNb = 160;
+// generation ever holds arrivals of two pairs, also once a role has given up (a failed wait: it
+// skips its work but meets every generation).  Both sides meet the generations in one order.
+constexpr uint32_t NB_LD = 1, NB_P = 2, NB_DS = 3, kNb = 256 + 32;
 
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kThreadsKv, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -263,7 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   const int hk = bh % a.Hkv, b = bh / a.Hkv;
   const long long kv_plane = (long long)b * a.Hkv + hk;
   const int N = g * (T - jt);   // pairs; the last g of them are the diagonal tile
-  const int M = 2 * N;          // sub-tiles
   auto hq_of = [&](int n) { return hk * g + n % g; };
   auto it_of = [&](int n) { return T - 1 - n / g; };
 
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         }
       }
       // stage n % 2 takes pair n + 2 once the MMAs of pair n have completed: they were its last
-      // readers, and the softmax warps were done with its statistics before its last dK
+      // readers, and the softmax warps were done with its statistics before its dK
       for (int n = 0; ok && n + 2 < N; ++n) {
         if (!(ok = mbar_wait(bar(KB_PD + (n & 1)), (uint32_t)(n >> 1) & 1u, ctl, W_PROD))) break;
         load_pair(n + 2);
@@ -335,29 +339,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   } else if (warp == 1) {
     // ======================= MMA issuer: lane 0 issues, the whole warp meets the named barriers
     bool ok = start_ok;
-    if (lane == 0 && ok) {   // Kh and Vt into TMEM (nothing is in flight yet: this wait drains nothing)
-      ok = mbar_wait(bar(KB_KV), 0, ctl, W_MMA_LD);
-      if (ok) {
-        tc_fence_after();
-        tile_to_tmem(tmem + T_KH, sbase + KV_KH);
-        tile_to_tmem(tmem + T_VH, sbase + KV_VH);
-      }
-    }
+    if (lane == 0 && ok) ok = mbar_wait(bar(KB_KV), 0, ctl, W_MMA_LD);   // nothing in flight yet
     ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
     auto live = [&]() { return ok && *abort_flag == 0; };
+    const uint64_t dKk = desc_kmajor_sw128(sbase + KV_KH), dVk = desc_kmajor_sw128(sbase + KV_VH);
     const uint64_t dQk = desc_kmajor_sw128(sbase + KV_QH), dDOk = desc_kmajor_sw128(sbase + KV_DO);
     const uint64_t dQm = smem_desc(sbase + KV_QH, ATOM, 1024, 2), dDOm = smem_desc(sbase + KV_DO, ATOM, 1024, 2);
-    constexpr uint32_t idN64 = idesc_bf16(BN, 64), idMN = idesc_bf16(BN, HD) | (1u << 16);
-    // sub-tile m reads stage (m / 2) % 2, query rows 64 (m % 2)..: descriptor start offsets (16-byte
-    // units) of its rows read along d (K-major) and along q (MN-major)
-    auto koff = [](int m) { return (uint32_t)((((m >> 1) & 1) * TILE + (m & 1) * 64 * 128) >> 4); };
-    auto moff = [](int m) { return (uint32_t)((((m >> 1) & 1) * TILE + (m & 1) * 4 * 2048) >> 4); };
-    auto issue_s = [&](int m) {
-      mma_ts<8, false>(tmem + T_ST, tmem + T_KH, dQk + koff(m), idN64, 0u);
+    constexpr uint32_t idN = idesc_bf16(BN, BM), idMN = idesc_bf16(BN, HD) | (1u << 16);
+    auto stg = [](int n) { return (uint32_t)(((n & 1) * TILE) >> 4); };
+    // D = A B^T over d, both K-major in shared memory
+    auto mma_ss = [&](uint32_t d, uint64_t da, uint64_t db) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t off = (uint32_t)(((s >> 2) * ATOM + (s & 3) * 32) >> 4);
+        mma_f16_ss(d, da + off, db + off, idN, s > 0 ? 1u : 0u);
+      }
+    };
+    // D (+)= A B over the pair's 128 queries: A in TMEM at columns 0-31 (queries 0-63) and 64-95
+    // (queries 64-127), B read along q
+    auto mma_q = [&](uint32_t d, uint32_t t_a, uint64_t db, uint32_t acc0) {
+      mma_ts<4, true>(d, t_a, db, idMN, acc0);
+      mma_ts<4, true>(d, t_a + 64, db + 4 * (2048 >> 4), idMN, 1u);
+    };
+    auto issue_s = [&](int n) {
+      mma_ss(tmem + T_ST, dKk, dQk + stg(n));
       tc_commit(bar(KB_SF));
     };
-    auto issue_dp = [&](int m) {
-      mma_ts<8, false>(tmem + T_DPT, tmem + T_VH, dDOk + koff(m), idN64, 0u);
+    auto issue_dp = [&](int n) {
+      mma_ss(tmem + T_DPT, dVk, dDOk + stg(n));
       tc_commit(bar(KB_DP));
     };
     named_sync(NB_LD, kNb);
@@ -367,53 +376,56 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       issue_dp(0);
     }
     __syncwarp();
-    for (int m = 0; m < M; ++m) {
+    for (int n = 0; n < N; ++n) {
       named_sync(NB_P, kNb);
       if (lane == 0 && live()) {   // dV += P^T dO
         tc_fence_after();
-        mma_ts<4, true>(tmem + T_DV, tmem + T_ST, dDOm + moff(m), idMN, m > 0 ? 1u : 0u);
+        mma_q(tmem + T_DV, tmem + T_ST, dDOm + stg(n), n > 0 ? 1u : 0u);
       }
       __syncwarp();
-      if (m + 1 < M) {
-        if (m & 1) named_sync(NB_LD, kNb);   // the next pair's data
+      if (n + 1 < N) {
+        named_sync(NB_LD, kNb);   // the next pair's data
         if (lane == 0 && live()) {
           tc_fence_after();
-          issue_s(m + 1);
+          issue_s(n + 1);
         }
         __syncwarp();
       }
       named_sync(NB_DS, kNb);
       if (lane == 0 && live()) {   // dK += dS^T Qh
         tc_fence_after();
-        mma_ts<4, true>(tmem + T_DK, tmem + T_DPT, dQm + moff(m), idMN, m > 0 ? 1u : 0u);
-        if (m & 1) tc_commit(bar(KB_PD + ((m >> 1) & 1)));
-        if (m + 1 < M) issue_dp(m + 1);
+        mma_q(tmem + T_DK, tmem + T_DPT, dQm + stg(n), n > 0 ? 1u : 0u);
+        tc_commit(bar(KB_PD + (n & 1)));
+        if (n + 1 < N) issue_dp(n + 1);
       }
       __syncwarp();
     }
     if (lane == 0) tc_commit(bar(KB_DRAIN));   // every MMA of the CTA
     __syncwarp();
   } else if (warp >= 4) {
-    // ======================= softmax: key row kr of the tile per thread
-    const int qq = warp & 3, kr = qq * 32 + lane;
+    // ======================= softmax: key row kr of the tile per thread, queries 64 h.. of it
+    const int qq = warp & 3, kr = qq * 32 + lane, h = (warp - 4) >> 2;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const uint32_t col = 64 * h;   // this warp's columns of S^T and dP^T
     const float sl2 = a.scale_log2e;
     bool ok = start_ok;
-    auto landed = [&](int n) {   // pair n's data landed; then its generation of NB_LD
+    // pair n's data landed; then its generation of NB_LD.  The first is met blocking: the arrival
+    // for pair 1 then follows the MMA warp's passing of pair 0's generation also when a wait failed.
+    auto landed = [&](int n) {
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_LF + (n & 1)), (uint32_t)(n >> 1) & 1u, ctl, W_SM_LD));
-      named_arrive(NB_LD, kNb);
+      if (n == 0) named_sync(NB_LD, kNb);
+      else named_arrive(NB_LD, kNb);
     };
-    auto sub = [&](int m, auto diag_tag) {
+    auto pair = [&](int n, auto diag_tag) {
       constexpr bool DIAG = decltype(diag_tag)::value;
-      const int h = m & 1;
-      const float* dlt = reinterpret_cast<const float*>(smem + KV_STAT + ((m >> 1) & 1) * 1024) + 64 * h;
+      const float* dlt = reinterpret_cast<const float*>(smem + KV_STAT + (n & 1) * 1024) + 64 * h;
       const float* lse2 = dlt + 128;
-      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_SF), (uint32_t)m & 1u, ctl, W_SM_S));
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_SF), (uint32_t)n & 1u, ctl, W_SM_S));
       float p[64];
       if (ok) {
         tc_fence_after();
-        tld32(tmem + lane_off + T_ST, p);
-        tld32(tmem + lane_off + T_ST + 32, p + 32);
+        tld32(tmem + lane_off + T_ST + col, p);
+        tld32(tmem + lane_off + T_ST + col + 32, p + 32);
         tmem_ld_wait();
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4) {
@@ -431,24 +443,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(p[32 * c + 2 * i], p[32 * c + 2 * i + 1]);
-          tst16(tmem + lane_off + T_ST + 16 * c, w);
+          tst16(tmem + lane_off + T_ST + col + 16 * c, w);
         }
         tmem_st_wait();
         tc_fence_before();
       }
       named_arrive(NB_P, kNb);
-      if ((m & 1) && m + 1 < M) landed((m + 1) >> 1);
-      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_DP), (uint32_t)m & 1u, ctl, W_SM_DP));
+      if (n + 1 < N) landed(n + 1);
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(KB_DP), (uint32_t)n & 1u, ctl, W_SM_DP));
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {   // dS^T of queries 32c.. over columns 16c.., read by then
+        for (int c = 0; c < 2; ++c) {   // dS^T of queries 64 h + 32 c.. over columns 64 h + 16 c.., read by then
           float d[32];
           uint32_t w[16];
-          tld32(tmem + lane_off + T_DPT + 32 * c, d);
+          tld32(tmem + lane_off + T_DPT + col + 32 * c, d);
           tmem_ld_wait();
           ds_chunk(p + 32 * c, d, dlt + 32 * c, w);
-          tst16(tmem + lane_off + T_DPT + 16 * c, w);
+          tst16(tmem + lane_off + T_DPT + col + 16 * c, w);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -456,9 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       named_sync(NB_DS, kNb);
     };
     landed(0);
-    int m = 0;
-    for (; m < 2 * (N - g); ++m) sub(m, std::false_type{});
-    for (; m < M; ++m) sub(m, std::true_type{});
+    int n = 0;
+    for (; n < N - g; ++n) pair(n, std::false_type{});
+    for (; n < N; ++n) pair(n, std::true_type{});
   }
 
   // ======================= epilogue: dV and dK from TMEM, 8 warps
@@ -466,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   __syncthreads();
   const bool drained = mbar_wait_drain(bar(KB_DRAIN), 0, a.limit_ns);
   tc_fence_after();
-  if (cta_all(drained && start_ok && *abort_flag == 0)) {
+  if (cta_all(drained && start_ok && *abort_flag == 0) && warp < 8) {
     store_acc(tmem + T_DV, a.dv, a, a.Hkv, b, hk, jt, 1.0f);
     store_acc(tmem + T_DK, a.dk, a, a.Hkv, b, hk, jt, a.scale);
   }
@@ -748,7 +760,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st) {
   attn_bwd_dq_kernel<<<(unsigned)((long long)args.B * args.Hq * T), kThreadsDq, QQ_SMEM, st>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_kernel<<<(unsigned)((long long)args.B * args.Hkv * T), kThreads, KV_SMEM, st>>>(args);
+  attn_bwd_dkdv_kernel<<<(unsigned)((long long)args.B * args.Hkv * T), kThreadsKv, KV_SMEM, st>>>(args);
   return cudaGetLastError();
 }
 

@@ -56,7 +56,81 @@ __device__ __forceinline__ uint2 quant8(const uint4& v, float inv, bool nonfinit
 // block is 4 adjacent threads.  Each thread loads its four chunks (rows s0 + 16i + tid/16) before
 // converting any, so that 64 bytes per thread are in flight.  Scales are compact: the four scale
 // bytes of token s (blocks c = d/32) form one 32-bit word at sc[((b*H + h)*S + s)*4 + c].
-constexpr int RW_ROWS = 64;
+#define BSC_QUANT_MINB 5   // resident CTAs per SM the register budget is sized for
+constexpr int RW_LOADS = 4;                  // 16-byte loads in flight per thread
+constexpr int RW_ROWS = 16 * RW_LOADS;       // token rows per CTA
+
+// One token row's 8 elements held by this thread (16 threads per row, a 32-element block is 4
+// adjacent threads): block amax, scale, E4M3 bytes to q[e..], and the row's scale word from its
+// first thread.  Every thread of the warp takes part (the shuffles).
+__device__ __forceinline__ void rowwise_emit(const uint4& v, int s, int S, long long e, long long plane,
+                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int rule, int lane,
+                                             int l16) {
+  uint32_t am = absmax_bits8(v);
+  am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+  am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+  float inv;
+  const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
+  if (s < S) __stcs(reinterpret_cast<uint2*>(q + e), quant8(v, inv, sb == 0xFFu));
+  // gather the 4 block scales of this row on its first thread
+  const int base = lane & 16;
+  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, base + 4);
+  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 8);
+  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 12);
+  if (s < S && l16 == 0) {
+    *reinterpret_cast<uint32_t*>(sc + (plane * S + s) * 4) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  }
+}
+// The token-normalised copy of one V row (16 threads, 8 elements each; the row valid): one scale
+// for the whole row, vtn_sc[row_sc].  Every thread of the 16 takes part (the shuffles).
+__device__ __forceinline__ void token_norm_emit(const uint4& v, long long e, long long row_sc, uint8_t* vtn,
+                                                uint8_t* vtn_sc, int rule, int l16) {
+  uint32_t am = absmax_bits8(v);
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+  float inv;
+  const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
+  __stcs(reinterpret_cast<uint2*>(vtn + e), quant8(v, inv, sb == 0xFFu));
+  if (l16 == 0) vtn_sc[row_sc] = (uint8_t)sb;
+}
+// The columnwise copy of one 32-token block for two columns d0 = 2 dp, d0 + 1: the block's bf16
+// values at col + r * pitch (r < 32, the pair as one 32-bit word); writes the 32 bytes of each
+// column to vt (transposed: row (plane * 128 + d) of S bytes, tokens s_blk..) and the two scale
+// bytes to vsc[blk_idx * 128 + d0].  Two passes over the block (the amax, then the bytes) keep no
+// column in registers.
+__device__ __forceinline__ void colwise_emit(const uint8_t* col, int pitch, long long plane, int dp, int s_blk,
+                                             long long blk_idx, int S, uint8_t* vt, uint8_t* vsc, int rule) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(col + r * pitch) & 0x7FFF7FFFu;
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
+  }
+  float inv0, inv1;
+  const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0, rule);
+  const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1, rule);
+  const float2 inv2 = make_float2(inv0, inv1);   // column d0 in the low halves, d1 in the high
+  // word i of a column's 32-token block holds tokens 4i..4i+3 (natural order)
+  uint32_t o0[8], o1[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float2 t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) t[u] = scale_bf16x2(*reinterpret_cast<const uint32_t*>(col + (4 * i + u) * pitch), inv2);
+    const uint32_t lo0 = cvt_e4m3x2(t[0].x, t[1].x), hi0 = cvt_e4m3x2(t[2].x, t[3].x);
+    const uint32_t lo1 = cvt_e4m3x2(t[0].y, t[1].y), hi1 = cvt_e4m3x2(t[2].y, t[3].y);
+    o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu : (lo0 | (hi0 << 16));
+    o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
+  }
+  const int d0 = 2 * dp, d1 = 2 * dp + 1;
+  uint8_t* row0 = vt + (plane * 128 + d0) * S + s_blk;
+  uint8_t* row1 = vt + (plane * 128 + d1) * S + s_blk;
+  __stcs(reinterpret_cast<uint4*>(row0), make_uint4(o0[0], o0[1], o0[2], o0[3]));
+  __stcs(reinterpret_cast<uint4*>(row0) + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
+  __stcs(reinterpret_cast<uint4*>(row1), make_uint4(o1[0], o1[1], o1[2], o1[3]));
+  __stcs(reinterpret_cast<uint4*>(row1) + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
+  *reinterpret_cast<uint16_t*>(vsc + blk_idx * 128 + d0) = (uint16_t)(sb0 | (sb1 << 8));
+}
 
 // `blk` = plane * ceil(S/64) + s-chunk.
 __device__ __forceinline__ void rowwise_rows(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
@@ -69,35 +143,19 @@ __device__ __forceinline__ void rowwise_rows(const uint8_t* __restrict__ x, uint
   const long long row_stride = layout == 0 ? (long long)H * 128 : (long long)B * H * 128;   // elements per s
   const long long base0 = layout == 0 ? ((b * S) * H + h) * 128 : (b * H + h) * 128;
   const int tid = threadIdx.x, l16 = tid & 15, lane = tid & 31;
-  uint4 v[4];
-  long long e[4];
+  uint4 v[RW_LOADS];
+  long long e[RW_LOADS];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < RW_LOADS; ++i) {
     const int s = s0 + 16 * i + (tid >> 4);
     e[i] = base0 + (long long)s * row_stride + l16 * 8;
     v[i] = s < S ? __ldcs(reinterpret_cast<const uint4*>(x + e[i] * 2)) : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int s = s0 + 16 * i + (tid >> 4);
-    uint32_t am = absmax_bits8(v[i]);
-    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-    float inv;
-    const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
-    if (s < S) __stcs(reinterpret_cast<uint2*>(q + e[i]), quant8(v[i], inv, sb == 0xFFu));
-    // gather the 4 block scales of this row on its first thread
-    const int base = lane & 16;
-    const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, base + 4);
-    const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 8);
-    const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 12);
-    if (s < S && l16 == 0) {
-      *reinterpret_cast<uint32_t*>(sc + (plane * S + s) * 4) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-    }
-  }
+  for (int i = 0; i < RW_LOADS; ++i) rowwise_emit(v[i], s0 + 16 * i + (tid >> 4), S, e[i], plane, q, sc, rule, lane, l16);
 }
 
-__global__ void __launch_bounds__(256, 5) quant_rowwise_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
+__global__ void __launch_bounds__(256, BSC_QUANT_MINB) quant_rowwise_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
                                                             uint8_t* __restrict__ sc, int B, int S, int H,
                                                             int layout, int rule) {
   rowwise_rows(x, q, sc, B, S, H, layout, rule, blockIdx.x);
@@ -136,61 +194,21 @@ __device__ __forceinline__ void v_tile(const uint8_t* __restrict__ v, uint8_t* _
     const long long e = base0 + (long long)(s0 + r) * row_stride + l16 * 8;
     const uint4 val = valid ? __ldcs(reinterpret_cast<const uint4*>(v + e * 2)) : make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(&tile[r * VQ_PITCH + l16 * 16]) = val;
-    if (vtn != nullptr && valid) {
-      // token-normalised copy straight from registers: the 16 threads of a row reduce its amax
-      uint32_t am = absmax_bits8(val);
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
-      float inv;
-      const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
-      __stcs(reinterpret_cast<uint2*>(vtn + e), quant8(val, inv, sb == 0xFFu));
-      if (l16 == 0) vtn_sc[(long long)plane * S + s0 + r] = (uint8_t)sb;
-    }
+    // token-normalised copy straight from registers: the 16 threads of a row reduce its amax
+    if (vtn != nullptr && valid) token_norm_emit(val, e, (long long)plane * S + s0 + r, vtn, vtn_sc, rule, l16);
   }
   if (vt == nullptr) return;
   __syncthreads();
 
-  // columnwise: thread -> (pair of d columns, 32-token block).  Two passes over the staged tile
-  // (the block amax, then the bytes) keep no column in registers.
+  // columnwise: thread -> (pair of d columns, 32-token block)
   const int dp = tid & 63;      // d = 2*dp, 2*dp + 1
   const int kb = tid >> 6;      // 32-token block inside the tile
-  const uint8_t* col = &tile[kb * 32 * VQ_PITCH + dp * 4];
-  uint32_t m = 0;
-#pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(col + r * VQ_PITCH) & 0x7FFF7FFFu;
-    asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
-  }
-  float inv0, inv1;
-  const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0, rule);
-  const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1, rule);
-  const float2 inv2 = make_float2(inv0, inv1);   // column d0 in the low halves, d1 in the high
-  // word i of a column's 32-token block holds tokens 4i..4i+3 (natural order)
-  uint32_t o0[8], o1[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float2 t[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) t[u] = scale_bf16x2(*reinterpret_cast<const uint32_t*>(col + (4 * i + u) * VQ_PITCH), inv2);
-    const uint32_t lo0 = cvt_e4m3x2(t[0].x, t[1].x), hi0 = cvt_e4m3x2(t[2].x, t[3].x);
-    const uint32_t lo1 = cvt_e4m3x2(t[0].y, t[1].y), hi1 = cvt_e4m3x2(t[2].y, t[3].y);
-    o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu : (lo0 | (hi0 << 16));
-    o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
-  }
-  const int d0 = 2 * dp, d1 = 2 * dp + 1;
-  if (s0 + kb * 32 < S) {   // whole 32-token blocks
-    uint8_t* row0 = vt + ((long long)plane * 128 + d0) * S + s0 + kb * 32;
-    uint8_t* row1 = vt + ((long long)plane * 128 + d1) * S + s0 + kb * 32;
-    __stcs(reinterpret_cast<uint4*>(row0), make_uint4(o0[0], o0[1], o0[2], o0[3]));
-    __stcs(reinterpret_cast<uint4*>(row0) + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
-    __stcs(reinterpret_cast<uint4*>(row1), make_uint4(o1[0], o1[1], o1[2], o1[3]));
-    __stcs(reinterpret_cast<uint4*>(row1) + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
-    const long long blk_idx = (long long)plane * (S / 32) + s0 / 32 + kb;
-    *reinterpret_cast<uint16_t*>(vsc + blk_idx * 128 + d0) = (uint16_t)(sb0 | (sb1 << 8));
-  }
+  if (s0 + kb * 32 < S)   // whole 32-token blocks
+    colwise_emit(&tile[kb * 32 * VQ_PITCH + dp * 4], VQ_PITCH, plane, dp, s0 + kb * 32,
+                 (long long)plane * (S / 32) + s0 / 32 + kb, S, vt, vsc, rule);
 }
 
-__global__ void __launch_bounds__(256, 5) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+__global__ void __launch_bounds__(256, BSC_QUANT_MINB) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
                                                       uint8_t* __restrict__ vsc, uint8_t* __restrict__ vtn,
                                                       uint8_t* __restrict__ vtn_sc, int B, int S, int H,
                                                       int layout, int rule) {
@@ -201,7 +219,7 @@ __global__ void __launch_bounds__(256, 5) quant_v_kernel(const uint8_t* __restri
 // ------------------------------------------------------------------------------------------
 // Q, K and V in one launch: CTAs [0, nv) take V tiles, then Q's 64-token chunks, then K's.  Each
 // CTA does exactly what the matching kernel above does for the same index.
-__global__ void __launch_bounds__(256, 5) quant_qkv_kernel(const __grid_constant__ QkvQuantArgs a) {
+__global__ void __launch_bounds__(256, BSC_QUANT_MINB) quant_qkv_kernel(const __grid_constant__ QkvQuantArgs a) {
   __shared__ __align__(16) uint8_t tile[VQ_ROWS * VQ_PITCH];
   const long long blk = blockIdx.x;
   if (blk < a.nv_blocks) {
