@@ -7,18 +7,19 @@
 //   P = exp(s - LSE),  dV = P^T dO,  dP = dO Vt^T,  Dlt = rowsum(dO * O),  dS = P * (dP - Dlt),
 //   dQ = scale * dS Kh,  dK = scale * dS^T Qh;  a KV head's dK, dV sum over its query heads.
 //
-// Three kernels:
+// Two launches:
 //   * prep: decodes Qh, Kh and Vt to BF16 planes [B][H][Sp][D] in the caller's workspace (rows
 //     past S zero) and writes the row statistics Dlt and LSE log2(e) there, once per call;
-//   * dK/dV: one CTA per (batch, KV head, 128-key tile); walks the group's (query head, query
-//     tile) pairs at or after the key tile, accumulating dV and dK in tensor memory;
-//   * dQ: one CTA per (batch, query head, 128-row query tile); walks the key tiles up to the
-//     diagonal, accumulating dQ in tensor memory.
-// Both attention kernels are warp-specialised (256 threads): warp 0 lane 0 issues the copies, warp 1
-// lane 0 the MMAs, warps 4-7 compute P and dS, one TMEM lane (row) per thread; warps 2-3 take part
-// in the epilogue only.  Every MMA is BF16 with its A operand in tensor memory (the tile the CTA
-// keeps, copied there once, or P / dS written there by the softmax warps) and its B operand in
-// shared memory, so the operand traffic through shared memory is one tile per MMA.  Every tile
+//   * one grid of two CTA roles:
+//     - dK/dV: one CTA per (batch, KV head, 128-key tile); walks the group's (query head, query
+//       tile) pairs at or after the key tile, accumulating dV and dK in tensor memory;
+//     - dQ: one CTA per (batch, query head, 128-row query tile); walks the key tiles up to the
+//       diagonal, accumulating dQ in tensor memory.
+// Both roles are warp-specialised (384 threads): warp 0 lane 0 issues the copies, warp 1 lane 0 the
+// MMAs, warps 4-11 compute P and dS (two warps per TMEM lane quarter, each with half the columns of
+// its rows); warps 2-3 take part in the epilogue only.  Every MMA is BF16.  P and dS reach their MMAs
+// from tensor memory (written there by the softmax warps); dQ keeps Qh and dO in tensor memory as
+// A operands, dK/dV keeps Kh and Vt in shared memory (so that its S^T and dP^T get N = 128).  Every tile
 // sits in shared memory in its natural orientation ([row][column], 64-column blocks with the
 // 128-byte swizzle); the products that contract over its rows (P^T dO, dS^T Qh, dS Kh) read it as
 // an MN-major operand, so nothing is transposed.  Every mbarrier wait is bounded; the MMA-issuing
@@ -37,7 +38,6 @@ namespace {
 constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // keys per tile
 constexpr int HD = 128;   // head dimension
-constexpr int kThreads = 256;
 constexpr uint32_t ATOM = 128 * 128;   // one 128-row x 128-byte swizzle block (64 BF16 columns)
 constexpr uint32_t TILE = 2 * ATOM;    // a 128 x 128 BF16 tile
 static_assert(BM == 128 && BN == 128 && HD == 128, "tile shapes assumed by the tensor-memory layouts");
@@ -251,7 +251,9 @@ static_assert(KB_COUNT * 8 <= 128, "barrier slots");
 // skips its work but meets every generation).  Both sides meet the generations in one order.
 constexpr uint32_t NB_LD = 1, NB_P = 2, NB_DS = 3, kNb = 256 + 32;
 
-__global__ void __launch_bounds__(kThreadsKv, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+// One dK/dV CTA; `cta` is its index among them.  `a` is the kernel's grid-constant parameter (the
+// tensor maps are read from there).
+__device__ __forceinline__ void dkdv_cta(const BwdArgs& a, int cta) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -263,8 +265,8 @@ __global__ void __launch_bounds__(kThreadsKv, 1) attn_bwd_dkdv_kernel(const __gr
   const int T = (a.S + BN - 1) / BN;
   const int g = a.Hq / a.Hkv;
   // key tiles with the most query tiles first
-  const int bh = blockIdx.x % (a.B * a.Hkv);
-  const int jt = (int)(blockIdx.x / (a.B * a.Hkv));
+  const int bh = cta % (a.B * a.Hkv);
+  const int jt = cta / (a.B * a.Hkv);
   const int hk = bh % a.Hkv, b = bh / a.Hkv;
   const long long kv_plane = (long long)b * a.Hkv + hk;
   const int N = g * (T - jt);   // pairs; the last g of them are the diagonal tile
@@ -527,7 +529,8 @@ constexpr int kThreadsDq = 384;
 constexpr uint32_t kNbDq = 256 + 32;
 constexpr uint32_t NB_S = 2;
 
-__global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+// One dQ CTA; `cta` is its index among them.
+__device__ __forceinline__ void dq_cta(const BwdArgs& a, int cta) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -537,8 +540,8 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int T = (a.S + BM - 1) / BM;
-  const int bh = blockIdx.x % (a.B * a.Hq);
-  const int it = T - 1 - (int)(blockIdx.x / (a.B * a.Hq));   // heaviest query tiles first
+  const int bh = cta % (a.B * a.Hq);
+  const int it = T - 1 - cta / (a.B * a.Hq);   // heaviest query tiles first
   const int hq = bh % a.Hq, b = bh / a.Hq;
   const int hk = hq / (a.Hq / a.Hkv);
   const long long kv_plane = (long long)b * a.Hkv + hk, q_plane = (long long)b * a.Hq + hq;
@@ -736,6 +739,19 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+
+// dK/dV and dQ in one grid: the dK/dV CTAs (heaviest key tiles first), then the dQ CTAs (heaviest
+// query tiles first).  The two are independent once the prep kernel has run; in one grid the CTAs
+// of one fill the SMs the other's last CTAs leave idle.
+static_assert(kThreadsKv == kThreadsDq, "one block size for both roles");
+constexpr uint32_t BWD_SMEM = KV_SMEM > QQ_SMEM ? KV_SMEM : QQ_SMEM;
+__global__ void __launch_bounds__(kThreadsKv, 1) attn_bwd_kernel(const __grid_constant__ BwdArgs a) {
+  const int T = (a.S + BN - 1) / BN;
+  const int nkv = a.B * a.Hkv * T;
+  if ((int)blockIdx.x < nkv) dkdv_cta(a, (int)blockIdx.x);
+  else dq_cta(a, (int)blockIdx.x - nkv);
+}
+
 }  // namespace
 
 size_t bwd_workspace_bytes(int B, int S, int Hq, int Hkv) {
@@ -746,9 +762,7 @@ size_t bwd_workspace_bytes(int B, int S, int Hq, int Hkv) {
 cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st) {
   static bool attr_set = false;   // the attribute is per function and per process
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QQ_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -757,10 +771,9 @@ cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t st) {
   attn_bwd_prep_kernel<<<dim3((unsigned)(args.Sp / 64), (unsigned)(args.B * args.Hq), 4), 256, 0, st>>>(args);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_kernel<<<(unsigned)((long long)args.B * args.Hq * T), kThreadsDq, QQ_SMEM, st>>>(args);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_kernel<<<(unsigned)((long long)args.B * args.Hkv * T), kThreadsKv, KV_SMEM, st>>>(args);
+  const long long ctas = (long long)args.B * (args.Hkv + args.Hq) * T;
+  if (ctas >= (1LL << 31)) return cudaErrorInvalidConfiguration;
+  attn_bwd_kernel<<<(unsigned)ctas, kThreadsKv, BWD_SMEM, st>>>(args);
   return cudaGetLastError();
 }
 
