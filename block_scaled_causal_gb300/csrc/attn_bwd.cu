@@ -193,12 +193,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t t_a, uint64_t b_desc
     mma_f16_ts(d, t_a + 8 * s, b_desc + off, idesc, s > 0 ? 1u : acc0);
   }
 }
-// dS = P (dP - Dlt) of 32 columns, packed to BF16 pairs.
+// dS = P (dP - Dlt) of 32 columns, packed to BF16 pairs (Dlt in 16-byte shared-memory loads, the
+// same address in every lane).
 __device__ __forceinline__ void ds_chunk(const float* p, const float* d, const float* dlt, uint32_t* w) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 dl = *reinterpret_cast<const float2*>(dlt + 2 * i);
-    w[i] = pack_bf16x2(p[2 * i] * (d[2 * i] - dl.x), p[2 * i + 1] * (d[2 * i + 1] - dl.y));
+  for (int i = 0; i < 8; ++i) {
+    const float4 dl = *reinterpret_cast<const float4*>(dlt + 4 * i);
+    w[2 * i] = pack_bf16x2(p[4 * i] * (d[4 * i] - dl.x), p[4 * i + 1] * (d[4 * i + 1] - dl.y));
+    w[2 * i + 1] = pack_bf16x2(p[4 * i + 2] * (d[4 * i + 2] - dl.z), p[4 * i + 3] * (d[4 * i + 3] - dl.w));
   }
 }
 
