@@ -79,9 +79,12 @@ def _run_and_check(ops, w, seed):
     return ", ".join(out)
 
 
+# S = 32 and 96: a single partial tile (every pair is the diagonal one); 160 and 288: a partial last
+# tile behind whole ones; 16/4-style grouping with 8/2
 @pytest.mark.parametrize("S,Hq,Hkv,layout,B", [(128, 2, 2, I.BSHD, 1), (256, 4, 2, I.BSHD, 1),
                                               (384, 2, 2, I.SBHD, 2), (160, 4, 2, I.BSHD, 1),
-                                              (512, 4, 1, I.BSHD, 1)])
+                                              (512, 4, 1, I.BSHD, 1), (32, 2, 1, I.BSHD, 1),
+                                              (96, 4, 4, I.SBHD, 2), (288, 8, 2, I.BSHD, 1)])
 def test_bwd_against_oracle(ops, S, Hq, Hkv, layout, B):
     w = I.Workload("bwd", B, S, Hq, Hkv, layout=layout)
     print(_run_and_check(ops, w, 80))
