@@ -110,10 +110,16 @@ enum Site : int {
 // Named barriers (ID 0 is __syncthreads):
 //   NB_KV      forwarder + MMA warp, once per key tile, both blocking: the stage's tiles landed and
 //              its scale atoms are written (the first generation covers the Q tile as well);
-//   NB_P + b   softmax warps (arrive) + MMA warp (sync): the P of the tile in S[b] and its scales
-//              are written.  Two IDs alternate with the tile parity: the scores of tile j + 2, and
-//              so its arrival, exist only after the MMA warp has passed tile j's generation.
-constexpr uint32_t NB_KV = 1, NB_P = 2;
+//   NB_P + (j mod 3)   softmax warps (arrive) + MMA warp (sync): the P of tile j and its scales are
+//              written.  Three IDs in turn: the scores of tile j + 2, and so its arrivals, exist
+//              only after the MMA warp has passed tile j's generation; and a softmax warp that
+//              gives up at tile j (a failed wait; it then blocks on every later generation) has
+//              arrived without waiting up to tile j - 1 at most, whose scores imply that the MMA
+//              warp has passed tile j - 3.  So no sync or arrival can ever join the generation of
+//              another tile.  With two IDs a warp giving up mid-run could join tile j - 2's
+//              generation while a slower warp had not yet arrived there, and a random-interleaving
+//              model of that protocol then deadlocked.
+constexpr uint32_t NB_KV = 1, NB_P = 2, kPIds = 3;
 constexpr uint32_t kNbP = 32 + 32 * kSoftmaxWarps;
 
 __device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
@@ -407,8 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       __syncwarp();
     }
+    uint32_t pid = NB_P;   // NB_P + j mod kPIds
     for (int j = 0; j <= t; ++j) {
-      named_sync(NB_P + (j & 1), kNbP);
+      named_sync(pid, kNbP);
+      pid = pid == NB_P + kPIds - 1 ? NB_P : pid + 1;
       if (lane == 0 && ok) {
         tc_fence_after();
         if (j < t) {
@@ -498,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // 2^(s - m) over the keys so far.
     float m = -INFINITY, l = 0.f;
     bool ok = start_ok;
+    uint32_t pid = NB_P;   // NB_P + j mod kPIds
     // One key tile.  The diagonal tile (DIAG) has its own instantiation, peeled out of the loop, so
     // that the loop body holds only the code of ordinary tiles.
     auto tile = [&](int j, auto diag_tag) {
@@ -608,10 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // arrive on a later generation before the MMA warp has passed this one)
       if (ok) {
         tc_fence_before();
-        named_arrive(NB_P + sb, kNbP);
+        named_arrive(pid, kNbP);
       } else {
-        named_sync(NB_P + sb, kNbP);
+        named_sync(pid, kNbP);
       }
+      pid = pid == NB_P + kPIds - 1 ? NB_P : pid + 1;
     };
     for (int j = 0; j < t; ++j) tile(j, std::false_type{});
     tile(t, std::true_type{});
