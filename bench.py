@@ -287,6 +287,42 @@ class Workload1:
         return ([a.elapsed_time(c) for a, _, c in evs], [b.elapsed_time(c) for _, b, c in evs],
                 [a.elapsed_time(b) for a, b, _ in evs])
 
+    def quant_alone(self, n=20, warm=3):
+        """The one-launch quantiser alone: the bytes it must move once (Q, K, V in; every output
+        out) over its CUDA-event time, after the 256 MB write flush the step uses and after a clean
+        flush (that write, then a 512 MB read, so that the L2 holds none of the workload and no dirty
+        lines); and a device copy of the same byte count after the clean flush, for scale."""
+        import torch
+        w, ops, st = self.w, self.ops, self.stream
+        rd = torch.ones(128 << 20, dtype=torch.int32, device=self.dev)
+        nbytes = sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v)) + sum(t.numel() for t in self.quant)
+        src = torch.ones(nbytes // 2, dtype=torch.uint8, device=self.dev)
+        dst = torch.empty_like(src)
+
+        def med_us(fn, pre):
+            evs = []
+            for i in range(warm + n):
+                pre()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                fn()
+                b.record(st)
+                if i >= warm:
+                    evs.append((a, b))
+            torch.cuda.synchronize()
+            ms = sorted(a.elapsed_time(b) for a, b in evs)
+            return 1e3 * ms[len(ms) // 2]
+
+        write_flush = lambda: self.flush.zero_()
+        clean_flush = lambda: (self.flush.zero_(), rd.sum())
+        quant = lambda: ops.mxfp8_quantize_qkv(self.q, self.k, self.v, w.layout, out=self.quant, stream=st)
+        res = {"bytes": nbytes,
+               "after_write_flush_us": med_us(quant, write_flush),
+               "after_clean_flush_us": med_us(quant, clean_flush),
+               "copy_same_bytes_after_clean_flush_us": med_us(lambda: dst.copy_(src), clean_flush)}
+        del rd, src, dst
+        return res
+
     def backward_ms(self, p_terms, steps, warmup):
         """The BF16 backward on operands decoded from this step's MXFP8 bytes (O and LSE of the
         forward, a synthetic dO), inputs resident; milliseconds per call."""
@@ -397,6 +433,8 @@ def main():
     s8, a8, _ = hb.timed(args.p_terms, max(3, args.steps // 2), 2, out8=True)
     ms8 = max_over_ranks(avg(s8), world, dev)
     attn8 = avg(a8)
+
+    qa = hb.quant_alone()
 
     # end to end through the public call with host buffers (pinned), copies inside the timed region.
     # Pipelined: step i's host->device copy runs on one copy stream while step i-1 computes, and its
@@ -535,6 +573,20 @@ def main():
                 "traffic_note": "traffic: ncu dram bytes per launch from the committed profile of this kernel "
                                 "source (null once the source differs); the estimate is the bytes the kernel "
                                 "must move once"}
+    gbs = lambda us: qa["bytes"] / (us * 1e-6) / 1e9
+    quant_roofline = {
+        "bound": "hbm", "kernel": "quant_qkv_kernel", "unit": "GB/s", "peak": hbm_peak, "bytes": qa["bytes"],
+        "achieved": gbs(qa["after_clean_flush_us"]), "frac": gbs(qa["after_clean_flush_us"]) / hbm_peak,
+        "us": qa["after_clean_flush_us"],
+        "after_write_flush": {"us": qa["after_write_flush_us"], "achieved": gbs(qa["after_write_flush_us"]),
+                              "frac": gbs(qa["after_write_flush_us"]) / hbm_peak},
+        "copy_same_bytes": {"us": qa["copy_same_bytes_after_clean_flush_us"],
+                            "achieved": gbs(qa["copy_same_bytes_after_clean_flush_us"]),
+                            "frac": gbs(qa["copy_same_bytes_after_clean_flush_us"]) / hbm_peak},
+        "note": "quantiser alone, median of 20 calls; achieved/frac after a clean flush (256 MB write then a "
+                "512 MB read: no workload data and no dirty lines in L2); after_write_flush is the step's own "
+                "flush, whose dirty lines are written back during the call; copy_same_bytes is a device copy "
+                "moving the same bytes after the clean flush; peak %s" % peak_kind}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         val, t_total, _ = run_oracle_steps(w, q_cpu, k_cpu, v_cpu, steps=6, warmup=0, rows_per_step=16)
@@ -558,6 +610,7 @@ def main():
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
         "quant_ms": avg(quant_ms),
+        "quant_roofline": quant_roofline,
         "attn_ms": attn_avg,
         "mxfp8_o": {"ms_per_step": ms8, "attn_ms": attn8, "value": whole_job_tflops(flops, world, ms8)},
         "configs": configs or None,

@@ -52,32 +52,35 @@ __device__ __forceinline__ uint2 quant8(const uint4& v, float inv, bool nonfinit
 
 // ------------------------------------------------------------------------------------------
 // Rowwise quantiser (Q, K): a CTA of 256 threads takes 64 consecutive tokens s0..s0+63 of one
-// (b, h) plane; a token row is 256 bytes = 16 threads x 16 bytes (8 elements) and a 32-element
-// block is 4 adjacent threads.  Each thread loads its four chunks (rows s0 + 16i + tid/16) before
+// (b, h) plane; a token row is 256 bytes = 8 threads x 32 bytes (16 elements) and a 32-element
+// block is 2 adjacent threads.  Each thread loads both of its rows (s0 + 32i + tid/8) before
 // converting any, so that 64 bytes per thread are in flight.  Scales are compact: the four scale
 // bytes of token s (blocks c = d/32) form one 32-bit word at sc[((b*H + h)*S + s)*4 + c].
 #define BSC_QUANT_MINB 5   // resident CTAs per SM the register budget is sized for
-constexpr int RW_LOADS = 4;                  // 16-byte loads in flight per thread
-constexpr int RW_ROWS = 16 * RW_LOADS;       // token rows per CTA
+constexpr int RW_PASSES = 2;                 // token rows per thread
+constexpr int RW_ROWS = 32 * RW_PASSES;      // token rows per CTA
 
-// One token row's 8 elements held by this thread (16 threads per row, a 32-element block is 4
+// One token row's 16 elements held by this thread (8 threads per row, a 32-element block is 2
 // adjacent threads): block amax, scale, E4M3 bytes to q[e..], and the row's scale word from its
 // first thread.  Every thread of the warp takes part (the shuffles).
-__device__ __forceinline__ void rowwise_emit(const uint4& v, int s, int S, long long e, long long plane,
-                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int rule, int lane,
-                                             int l16) {
-  uint32_t am = absmax_bits8(v);
+__device__ __forceinline__ void rowwise_emit(const uint4& v0, const uint4& v1, int s, int S, long long e,
+                                             long long plane, uint8_t* __restrict__ q, uint8_t* __restrict__ sc,
+                                             int rule, int lane, int l8) {
+  uint32_t am = max(absmax_bits8(v0), absmax_bits8(v1));
   am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-  am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
   float inv;
   const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
-  if (s < S) __stcs(reinterpret_cast<uint2*>(q + e), quant8(v, inv, sb == 0xFFu));
+  if (s < S) {
+    const bool nonfinite = sb == 0xFFu;
+    const uint2 lo = quant8(v0, inv, nonfinite), hi = quant8(v1, inv, nonfinite);
+    __stcs(reinterpret_cast<uint4*>(q + e), make_uint4(lo.x, lo.y, hi.x, hi.y));
+  }
   // gather the 4 block scales of this row on its first thread
-  const int base = lane & 16;
-  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, base + 4);
-  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 8);
-  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 12);
-  if (s < S && l16 == 0) {
+  const int base = lane & 24;
+  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, base + 2);
+  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, base + 4);
+  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, base + 6);
+  if (s < S && l8 == 0) {
     *reinterpret_cast<uint32_t*>(sc + (plane * S + s) * 4) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
   }
 }
@@ -142,17 +145,20 @@ __device__ __forceinline__ void rowwise_rows(const uint8_t* __restrict__ x, uint
   const long long h = plane % H, b = plane / H;
   const long long row_stride = layout == 0 ? (long long)H * 128 : (long long)B * H * 128;   // elements per s
   const long long base0 = layout == 0 ? ((b * S) * H + h) * 128 : (b * H + h) * 128;
-  const int tid = threadIdx.x, l16 = tid & 15, lane = tid & 31;
-  uint4 v[RW_LOADS];
-  long long e[RW_LOADS];
+  const int tid = threadIdx.x, l8 = tid & 7, lane = tid & 31;
+  uint4 v[2 * RW_PASSES];
+  long long e[RW_PASSES];
 #pragma unroll
-  for (int i = 0; i < RW_LOADS; ++i) {
-    const int s = s0 + 16 * i + (tid >> 4);
-    e[i] = base0 + (long long)s * row_stride + l16 * 8;
-    v[i] = s < S ? __ldcs(reinterpret_cast<const uint4*>(x + e[i] * 2)) : make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < RW_PASSES; ++i) {
+    const int s = s0 + 32 * i + (tid >> 3);
+    e[i] = base0 + (long long)s * row_stride + l8 * 16;
+    const uint4* src = reinterpret_cast<const uint4*>(x + e[i] * 2);
+    v[2 * i] = s < S ? __ldcs(src) : make_uint4(0, 0, 0, 0);
+    v[2 * i + 1] = s < S ? __ldcs(src + 1) : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
-  for (int i = 0; i < RW_LOADS; ++i) rowwise_emit(v[i], s0 + 16 * i + (tid >> 4), S, e[i], plane, q, sc, rule, lane, l16);
+  for (int i = 0; i < RW_PASSES; ++i)
+    rowwise_emit(v[2 * i], v[2 * i + 1], s0 + 32 * i + (tid >> 3), S, e[i], plane, q, sc, rule, lane, l8);
 }
 
 __global__ void __launch_bounds__(256, BSC_QUANT_MINB) quant_rowwise_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q,
