@@ -294,7 +294,7 @@ class Workload1:
         lines); and a device copy of the same byte count after the clean flush, for scale."""
         import torch
         w, ops, st = self.w, self.ops, self.stream
-        rd = torch.ones(128 << 20, dtype=torch.int32, device=self.dev)
+        rd = torch.ones(128 << 20, dtype=torch.float32, device=self.dev)   # summed in fp32: no temporary
         nbytes = sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v)) + sum(t.numel() for t in self.quant)
         src = torch.ones(nbytes // 2, dtype=torch.uint8, device=self.dev)
         dst = torch.empty_like(src)

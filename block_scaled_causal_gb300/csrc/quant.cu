@@ -84,17 +84,19 @@ __device__ __forceinline__ void rowwise_emit(const uint4& v0, const uint4& v1, i
     *reinterpret_cast<uint32_t*>(sc + (plane * S + s) * 4) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
   }
 }
-// The token-normalised copy of one V row (16 threads, 8 elements each; the row valid): one scale
-// for the whole row, vtn_sc[row_sc].  Every thread of the 16 takes part (the shuffles).
-__device__ __forceinline__ void token_norm_emit(const uint4& v, long long e, long long row_sc, uint8_t* vtn,
-                                                uint8_t* vtn_sc, int rule, int l16) {
-  uint32_t am = absmax_bits8(v);
+// The token-normalised copy of one V row (8 threads, 16 elements each; the row valid): one scale
+// for the whole row, vtn_sc[row_sc].  Every thread of the 8 takes part (the shuffles).
+__device__ __forceinline__ void token_norm_emit(const uint4& v0, const uint4& v1, long long e, long long row_sc,
+                                                uint8_t* vtn, uint8_t* vtn_sc, int rule, int l8) {
+  uint32_t am = max(absmax_bits8(v0), absmax_bits8(v1));
 #pragma unroll
-  for (int o = 1; o < 16; o <<= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+  for (int o = 1; o < 8; o <<= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
   float inv;
   const uint32_t sb = e8m0_from_amax(__uint_as_float(am << 16), inv, rule);
-  __stcs(reinterpret_cast<uint2*>(vtn + e), quant8(v, inv, sb == 0xFFu));
-  if (l16 == 0) vtn_sc[row_sc] = (uint8_t)sb;
+  const bool nonfinite = sb == 0xFFu;
+  const uint2 lo = quant8(v0, inv, nonfinite), hi = quant8(v1, inv, nonfinite);
+  __stcs(reinterpret_cast<uint4*>(vtn + e), make_uint4(lo.x, lo.y, hi.x, hi.y));
+  if (l8 == 0) vtn_sc[row_sc] = (uint8_t)sb;
 }
 // The columnwise copy of one 32-token block for two columns d0 = 2 dp, d0 + 1: the block's bf16
 // values at col + r * pitch (r < 32, the pair as one 32-bit word); writes the 32 bytes of each
@@ -191,17 +193,22 @@ __device__ __forceinline__ void v_tile(const uint8_t* __restrict__ v, uint8_t* _
   const long long row_stride = layout == 0 ? (long long)H * 128 : (long long)B * H * 128;   // elements per s
   const long long base0 = layout == 0 ? (((long long)b * S) * H + h) * 128 : ((long long)b * H + h) * 128;
 
-  // load: 16 threads per token row, 8 rows per pass of 128 threads... 2048 chunks / 256 threads
+  // load: 8 threads per token row (32 bytes each), 32 rows per pass of 256 threads; a warp's 4 rows
+  // are all valid or all not (S and s0 are multiples of 32)
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
+  for (int it = 0; it < 4; ++it) {
     const int c = it * 256 + tid;
-    const int r = c >> 4, l16 = c & 15;
-    const bool valid = s0 + r < S;   // uniform over the 16 threads of a row
-    const long long e = base0 + (long long)(s0 + r) * row_stride + l16 * 8;
-    const uint4 val = valid ? __ldcs(reinterpret_cast<const uint4*>(v + e * 2)) : make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(&tile[r * VQ_PITCH + l16 * 16]) = val;
-    // token-normalised copy straight from registers: the 16 threads of a row reduce its amax
-    if (vtn != nullptr && valid) token_norm_emit(val, e, (long long)plane * S + s0 + r, vtn, vtn_sc, rule, l16);
+    const int r = c >> 3, l8 = c & 7;
+    const bool valid = s0 + r < S;
+    const long long e = base0 + (long long)(s0 + r) * row_stride + l8 * 16;
+    const uint4* src = reinterpret_cast<const uint4*>(v + e * 2);
+    const uint4 v0 = valid ? __ldcs(src) : make_uint4(0, 0, 0, 0);
+    const uint4 v1 = valid ? __ldcs(src + 1) : make_uint4(0, 0, 0, 0);
+    uint4* dst = reinterpret_cast<uint4*>(&tile[r * VQ_PITCH + l8 * 32]);
+    dst[0] = v0;
+    dst[1] = v1;
+    // token-normalised copy straight from registers: the 8 threads of a row reduce its amax
+    if (vtn != nullptr && valid) token_norm_emit(v0, v1, e, (long long)plane * S + s0 + r, vtn, vtn_sc, rule, l8);
   }
   if (vt == nullptr) return;
   __syncthreads();
