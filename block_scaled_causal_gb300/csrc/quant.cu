@@ -98,43 +98,56 @@ __device__ __forceinline__ void token_norm_emit(const uint4& v0, const uint4& v1
   __stcs(reinterpret_cast<uint4*>(vtn + e), make_uint4(lo.x, lo.y, hi.x, hi.y));
   if (l8 == 0) vtn_sc[row_sc] = (uint8_t)sb;
 }
-// The columnwise copy of one 32-token block for two columns d0 = 2 dp, d0 + 1: the block's bf16
-// values at col + r * pitch (r < 32, the pair as one 32-bit word); writes the 32 bytes of each
-// column to vt (transposed: row (plane * 128 + d) of S bytes, tokens s_blk..) and the two scale
-// bytes to vsc[blk_idx * 128 + d0].  Two passes over the block (the amax, then the bytes) keep no
-// column in registers.
-__device__ __forceinline__ void colwise_emit(const uint8_t* col, int pitch, long long plane, int dp, int s_blk,
-                                             long long blk_idx, int S, uint8_t* vt, uint8_t* vsc, int rule) {
-  uint32_t m = 0;
+// The columnwise copy of one 32-token block for four columns d0 = 4 cq .. d0 + 3, this thread's half of
+// it: tokens 16 th .. 16 th + 15 at col + r * pitch (r < 16, the four columns' bf16 values as one
+// 64-bit word).  The block amax combines with the other half's thread (lane ^ 1).  Returns the 16
+// E4M3 bytes of each column's half in out[c] (tokens in natural order) and writes, from the th = 0
+// thread, the four scale bytes to vsc[blk_idx * 128 + d0].  Two passes over the rows (the amax, then
+// the bytes) keep no column in registers.
+__device__ __forceinline__ void colwise_emit(const uint8_t* col, int pitch, int th, long long blk_idx, int cq,
+                                             uint8_t* vsc, int rule, uint4 (&out)[4]) {
+  uint32_t m01 = 0, m23 = 0;
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(col + r * pitch) & 0x7FFF7FFFu;
-    asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
+  for (int r = 0; r < 16; ++r) {
+    const uint2 a = *reinterpret_cast<const uint2*>(col + r * pitch);
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m01) : "r"(a.x & 0x7FFF7FFFu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m23) : "r"(a.y & 0x7FFF7FFFu));
   }
-  float inv0, inv1;
-  const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m & 0xFFFFu) << 16), inv0, rule);
-  const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m & 0xFFFF0000u), inv1, rule);
-  const float2 inv2 = make_float2(inv0, inv1);   // column d0 in the low halves, d1 in the high
-  // word i of a column's 32-token block holds tokens 4i..4i+3 (natural order)
-  uint32_t o0[8], o1[8];
+  const uint32_t p01 = __shfl_xor_sync(0xFFFFFFFFu, m01, 1), p23 = __shfl_xor_sync(0xFFFFFFFFu, m23, 1);
+  asm("max.u16x2 %0, %0, %1;" : "+r"(m01) : "r"(p01));
+  asm("max.u16x2 %0, %0, %1;" : "+r"(m23) : "r"(p23));
+  float inv0, inv1, inv2, inv3;
+  const uint32_t sb0 = e8m0_from_amax(__uint_as_float((m01 & 0xFFFFu) << 16), inv0, rule);
+  const uint32_t sb1 = e8m0_from_amax(__uint_as_float(m01 & 0xFFFF0000u), inv1, rule);
+  const uint32_t sb2 = e8m0_from_amax(__uint_as_float((m23 & 0xFFFFu) << 16), inv2, rule);
+  const uint32_t sb3 = e8m0_from_amax(__uint_as_float(m23 & 0xFFFF0000u), inv3, rule);
+  const float2 inv01 = make_float2(inv0, inv1), inv23 = make_float2(inv2, inv3);
+  // word i of a column's 16 tokens holds tokens 4i..4i+3 (natural order)
+  uint32_t o0[4], o1[4], o2[4], o3[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float2 t[4];
+  for (int i = 0; i < 4; ++i) {
+    float2 t01[4], t23[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) t[u] = scale_bf16x2(*reinterpret_cast<const uint32_t*>(col + (4 * i + u) * pitch), inv2);
-    const uint32_t lo0 = cvt_e4m3x2(t[0].x, t[1].x), hi0 = cvt_e4m3x2(t[2].x, t[3].x);
-    const uint32_t lo1 = cvt_e4m3x2(t[0].y, t[1].y), hi1 = cvt_e4m3x2(t[2].y, t[3].y);
-    o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu : (lo0 | (hi0 << 16));
-    o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu : (lo1 | (hi1 << 16));
+    for (int u = 0; u < 4; ++u) {
+      const uint2 a = *reinterpret_cast<const uint2*>(col + (4 * i + u) * pitch);
+      t01[u] = scale_bf16x2(a.x, inv01);
+      t23[u] = scale_bf16x2(a.y, inv23);
+    }
+    o0[i] = sb0 == 0xFFu ? 0x7F7F7F7Fu
+                         : ((uint32_t)cvt_e4m3x2(t01[0].x, t01[1].x) | ((uint32_t)cvt_e4m3x2(t01[2].x, t01[3].x) << 16));
+    o1[i] = sb1 == 0xFFu ? 0x7F7F7F7Fu
+                         : ((uint32_t)cvt_e4m3x2(t01[0].y, t01[1].y) | ((uint32_t)cvt_e4m3x2(t01[2].y, t01[3].y) << 16));
+    o2[i] = sb2 == 0xFFu ? 0x7F7F7F7Fu
+                         : ((uint32_t)cvt_e4m3x2(t23[0].x, t23[1].x) | ((uint32_t)cvt_e4m3x2(t23[2].x, t23[3].x) << 16));
+    o3[i] = sb3 == 0xFFu ? 0x7F7F7F7Fu
+                         : ((uint32_t)cvt_e4m3x2(t23[0].y, t23[1].y) | ((uint32_t)cvt_e4m3x2(t23[2].y, t23[3].y) << 16));
   }
-  const int d0 = 2 * dp, d1 = 2 * dp + 1;
-  uint8_t* row0 = vt + (plane * 128 + d0) * S + s_blk;
-  uint8_t* row1 = vt + (plane * 128 + d1) * S + s_blk;
-  __stcs(reinterpret_cast<uint4*>(row0), make_uint4(o0[0], o0[1], o0[2], o0[3]));
-  __stcs(reinterpret_cast<uint4*>(row0) + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
-  __stcs(reinterpret_cast<uint4*>(row1), make_uint4(o1[0], o1[1], o1[2], o1[3]));
-  __stcs(reinterpret_cast<uint4*>(row1) + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
-  *reinterpret_cast<uint16_t*>(vsc + blk_idx * 128 + d0) = (uint16_t)(sb0 | (sb1 << 8));
+  // the column bytes go through shared memory (the caller's transposed tile), then out in whole rows
+  out[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+  out[1] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+  out[2] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  out[3] = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+  if (th == 0) *reinterpret_cast<uint32_t*>(vsc + blk_idx * 128 + 4 * cq) = sb0 | (sb1 << 8) | (sb2 << 16) | (sb3 << 24);
 }
 
 // `blk` = plane * ceil(S/64) + s-chunk.
@@ -173,10 +186,14 @@ __global__ void __launch_bounds__(256, BSC_QUANT_MINB) quant_rowwise_kernel(cons
 // V quantiser: one CTA per (b, h, 128-token tile), 256 threads (the last tile of a sequence may
 // hold fewer than 128 tokens, always whole 32-token blocks).  Produces either or both of
 //   * the columnwise copy, transposed: vt[((b*H + h)*D + d)*S + s], with compact scales, one byte
-//     per (b, h, 32-token block, d): vsc[((b*H + h)*(S/32) + s/32)*D + d];
+//     per (b, h, 32-token block, d): vsc[((b*H + h)*(S/32) + s/32)*D + d]; its bytes are
+//     transposed in shared memory (over the bf16 tile, once that is read) and written as whole
+//     rows of the tile's tokens;
 //   * the token-normalised copy in V's own layout with scales vtn_sc[(b*H + h)*S + s].
 constexpr int VQ_ROWS = 128;
 constexpr int VQ_PITCH = 256 + 16;   // bytes per staged token row
+constexpr int VT_PITCH = 128 + 16;   // bytes per d row of the transposed E4M3 tile (in the same buffer)
+static_assert(128 * VT_PITCH <= VQ_ROWS * VQ_PITCH, "transposed tile fits");
 
 // `blk` is the (b, h, tile) index; `tile` is VQ_ROWS x VQ_PITCH bytes of shared memory.  The
 // whole CTA takes part.
@@ -193,32 +210,61 @@ __device__ __forceinline__ void v_tile(const uint8_t* __restrict__ v, uint8_t* _
   const long long row_stride = layout == 0 ? (long long)H * 128 : (long long)B * H * 128;   // elements per s
   const long long base0 = layout == 0 ? (((long long)b * S) * H + h) * 128 : ((long long)b * H + h) * 128;
 
-  // load: 8 threads per token row (32 bytes each), 32 rows per pass of 256 threads; a warp's 4 rows
-  // are all valid or all not (S and s0 are multiples of 32)
+  // load: the whole tile into shared memory by asynchronous 16-byte copies (no registers held while
+  // they are in flight), 16 threads per token row; rows past S are filled with zeros
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
+  for (int it = 0; it < 8; ++it) {
     const int c = it * 256 + tid;
-    const int r = c >> 3, l8 = c & 7;
+    const int r = c >> 4, l16 = c & 15;
     const bool valid = s0 + r < S;
-    const long long e = base0 + (long long)(s0 + r) * row_stride + l8 * 16;
-    const uint4* src = reinterpret_cast<const uint4*>(v + e * 2);
-    const uint4 v0 = valid ? __ldcs(src) : make_uint4(0, 0, 0, 0);
-    const uint4 v1 = valid ? __ldcs(src + 1) : make_uint4(0, 0, 0, 0);
-    uint4* dst = reinterpret_cast<uint4*>(&tile[r * VQ_PITCH + l8 * 32]);
-    dst[0] = v0;
-    dst[1] = v1;
-    // token-normalised copy straight from registers: the 8 threads of a row reduce its amax
-    if (vtn != nullptr && valid) token_norm_emit(v0, v1, e, (long long)plane * S + s0 + r, vtn, vtn_sc, rule, l8);
+    const long long e = base0 + (long long)(valid ? s0 + r : s0) * row_stride + l16 * 8;
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&tile[r * VQ_PITCH + l16 * 16]);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(v + e * 2), "r"(valid ? 16 : 0)
+                 : "memory");
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  // token-normalised copy from the tile: 8 threads per token row (16 elements each), 32 rows per pass
+  if (vtn != nullptr) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int c = it * 256 + tid;
+      const int r = c >> 3, l8 = c & 7;
+      if (s0 + r < S) {   // a warp's 4 rows are all valid or all not (S and s0 are multiples of 32)
+        const uint4* src = reinterpret_cast<const uint4*>(&tile[r * VQ_PITCH + l8 * 32]);
+        const long long e = base0 + (long long)(s0 + r) * row_stride + l8 * 16;
+        token_norm_emit(src[0], src[1], e, (long long)plane * S + s0 + r, vtn, vtn_sc, rule, l8);
+      }
+    }
   }
   if (vt == nullptr) return;
-  __syncthreads();
 
-  // columnwise: thread -> (pair of d columns, 32-token block)
-  const int dp = tid & 63;      // d = 2*dp, 2*dp + 1
-  const int kb = tid >> 6;      // 32-token block inside the tile
-  if (s0 + kb * 32 < S)   // whole 32-token blocks
-    colwise_emit(&tile[kb * 32 * VQ_PITCH + dp * 4], VQ_PITCH, plane, dp, s0 + kb * 32,
-                 (long long)plane * (S / 32) + s0 / 32 + kb, S, vt, vsc, rule);
+  // columnwise: warp -> (half of the d columns, 32-token block); lane -> (4 columns, half a block)
+  const int w = tid >> 5, ln = tid & 31;
+  const int th = ln & 1;                    // tokens 16 th .. 16 th + 15 of the block
+  const int cq = (w & 1) * 16 + (ln >> 1);  // d = 4 cq .. 4 cq + 3
+  const int kb = w >> 1;                    // 32-token block inside the tile (uniform per warp)
+  const bool blk_ok = s0 + kb * 32 < S;     // whole 32-token blocks
+  uint4 out[4];
+  if (blk_ok)
+    colwise_emit(&tile[(kb * 32 + 16 * th) * VQ_PITCH + cq * 8], VQ_PITCH, th, (long long)plane * (S / 32) + s0 / 32 + kb,
+                 cq, vsc, rule, out);
+  __syncthreads();   // every bf16 row is read: the tile now takes the E4M3 bytes as [d][token]
+  if (blk_ok) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(&tile[(4 * cq + c) * VT_PITCH + kb * 32 + 16 * th]) = out[c];
+  }
+  __syncthreads();
+  // whole rows of vt: 8 threads per d row (16 bytes each), 32 rows per pass; only the tile's tokens
+  const int ntok = min(VQ_ROWS, S - s0);
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int d = it * 32 + (tid >> 3), seg = tid & 7;
+    if (seg * 16 < ntok)
+      __stcs(reinterpret_cast<uint4*>(vt + ((long long)plane * 128 + d) * S + s0 + seg * 16),
+             *reinterpret_cast<const uint4*>(&tile[d * VT_PITCH + seg * 16]));
+  }
 }
 
 __global__ void __launch_bounds__(256, BSC_QUANT_MINB) quant_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
