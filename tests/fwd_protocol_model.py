@@ -23,7 +23,9 @@ Semantics modelled:
 
 `n_pids` is the number of named-barrier IDs the P hand-over (softmax -> MMA warp) rotates through:
 3 as built; 2 (tile parity) is the earlier form, which the model shows can mix generations and
-deadlock once a wait gives up mid-run.
+deadlock once a wait gives up mid-run.  `mistake` plants a protocol error, so that the tests can show
+the model catches one: "no_stage_wait" (the producer refills a K/V stage without waiting for the
+scores that prove its last reader completed).
 """
 import random
 
@@ -61,7 +63,8 @@ class _MBar:
 
 
 class _World:
-    def __init__(self, t, own, seed, rescale_p, abort_p, n_pids):
+    def __init__(self, t, own, seed, rescale_p, abort_p, n_pids, mistake=None):
+        self.mistake = mistake
         self.rng = random.Random(seed)
         self.t, self.own, self.rescale_p, self.abort_p, self.n_pids = t, own, rescale_p, abort_p, n_pids
         self.aborted = False
@@ -164,7 +167,7 @@ def _producer(w):
     loaded = [0] * NST
     for j in range(t + 1):
         st = j % NST
-        if j >= 2:   # the scores of tile j - 2 are in: the stage's last reader has completed
+        if j >= 2 and w.mistake != "no_stage_wait":   # tile j - 2's scores: the stage's last reader is done
             ok = yield from w.wait("S_FULL%d" % (j & 1), ((j - 2) >> 1) & 1)
             if not ok:
                 break
@@ -297,9 +300,9 @@ def _softmax(w, q):
         w.read("O%d" % q, t + 1, "epilogue%d" % q)
 
 
-def run(t, own, seed, rescale_p=0.3, abort_p=0.0, n_pids=3, max_idle=200000):
+def run(t, own, seed, rescale_p=0.3, abort_p=0.0, n_pids=3, mistake=None, max_idle=200000):
     """One interleaving; raises ModelError on a violation or a deadlock."""
-    w = _World(t, own, seed, rescale_p, abort_p, n_pids)
+    w = _World(t, own, seed, rescale_p, abort_p, n_pids, mistake)
     roles = {"producer": _producer(w), "forwarder": _forwarder(w), "mma": _mma(w)}
     if own:
         roles["decoder"] = _decoder(w)
@@ -326,7 +329,7 @@ def run(t, own, seed, rescale_p=0.3, abort_p=0.0, n_pids=3, max_idle=200000):
             raise ModelError("deadlock: %s still running" % ", ".join(sorted(roles)))
 
 
-def count_failures(seeds, tiles=(0, 1, 2, 3, 5, 8), abort_ps=(0.0, 0.002, 0.02), n_pids=3):
+def count_failures(seeds, tiles=(0, 1, 2, 3, 5, 8), abort_ps=(0.0, 0.002, 0.02), n_pids=3, mistake=None):
     """Failures over seeds x tile counts x {own block, leaky} x abort rates; the first messages."""
     failures, first = 0, []
     for seed in range(seeds):
@@ -334,7 +337,7 @@ def count_failures(seeds, tiles=(0, 1, 2, 3, 5, 8), abort_ps=(0.0, 0.002, 0.02),
             for own in (True, False):
                 for ap in abort_ps:
                     try:
-                        run(t, own, seed * 1000 + t, abort_p=ap, n_pids=n_pids)
+                        run(t, own, seed * 1000 + t, abort_p=ap, n_pids=n_pids, mistake=mistake)
                     except ModelError as e:
                         failures += 1
                         if len(first) < 3:
