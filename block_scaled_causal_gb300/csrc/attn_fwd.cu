@@ -46,8 +46,11 @@ constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // keys per tile
 constexpr int HD = 128;   // head dimension
 constexpr int NST = 4;    // K/V shared-memory stages (the producer's wait rule assumes 4)
-constexpr int kThreads = 256;
-constexpr int kSoftmaxWarps = 4;
+// Softmax sets: with one E4M3 term for P, one set of four softmax warps takes every key tile; with two
+// terms (more exponent and convert work per tile) two sets of four take alternate tiles (set x the
+// tiles j with j mod 2 == x, so always S[x]), handing the running row maximum to each other.
+template <int P_TERMS> constexpr int kSets = P_TERMS == 2 ? 2 : 1;
+template <int P_TERMS> constexpr int kThreadsFor = 128 + 128 * kSets<P_TERMS>;
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t TILE8 = BM * HD;                      // one 128 x 128 E4M3 tile
@@ -64,7 +67,9 @@ constexpr uint32_t OFF_VATOM = OFF_KATOM + NST * 512;    // V scale atoms, NST s
 constexpr uint32_t OFF_BAR = OFF_VATOM + NST * 512;
 constexpr uint32_t NUM_BARS = 32;
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;    // tmem slot, abort flag
-constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t OFF_MROW = OFF_MISC + 16;             // per row: the running maximum last decided
+constexpr uint32_t OFF_LROW = OFF_MROW + 512;            // per row: set 1's part of the row sum
+constexpr uint32_t SMEM_USED = OFF_LROW + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;        // alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -120,7 +125,14 @@ enum Site : int {
 //              generation while a slower warp had not yet arrived there, and a random-interleaving
 //              model of that protocol then deadlocked.
 constexpr uint32_t NB_KV = 1, NB_P = 2, kPIds = 3;
-constexpr uint32_t kNbP = 32 + 32 * kSoftmaxWarps;
+constexpr uint32_t kNbP = 32 + 32 * 4;   // the MMA warp and the four softmax warps of the tile's set
+//   NB_M + (j mod 2)   (two sets) the set that owns tile j (arrive) + the other set (sync): the row
+//              maximum decided at tile j is in shared memory.  Each set takes the previous tile's
+//              decision before it publishes its own, so the decisions of consecutive tiles alternate
+//              between the two IDs and a generation never holds arrivals of two tiles.
+//   NB_L       (two sets) set 1 (arrive) + set 0 (sync): set 1's part of the row sum is in shared memory.
+constexpr uint32_t NB_M = 5, NB_L = 7, kNbM = 256;
+static_assert(NB_L < 16, "named barrier IDs");
 
 __device__ __forceinline__ float pow2_e8m0(uint32_t sb) {
   return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);   // 2^(sb-127), sb <= 254
@@ -251,7 +263,8 @@ __device__ __forceinline__ uint32_t block_p(float (&v)[128], const float (&bm)[4
 }
 
 template <int P_TERMS, bool LEAKY>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kThreadsFor<P_TERMS>, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int SETS = kSets<P_TERMS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -304,6 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   const bool start_ok = *abort_flag == 0;
 
+  // Two sets: the launch gives 168 registers per thread (384 x 168 = 64512); the four helper warps keep
+  // 112, the eight softmax warps get 192: 128 x 112 + 256 x 192 = 63488.
+  if (warp < 4) {
+  if constexpr (SETS == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
   if (warp == 0) {
     // ======================= producer
     if (lane == 0) {
@@ -496,24 +513,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       __syncwarp();
       named_sync(NB_KV, 64);
     }
+  }
   } else {
-    // ======================= softmax + epilogue: one query row per thread
+    if constexpr (SETS == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    // ======================= softmax + epilogue: one query row per thread; set x takes the key tiles
+    // j with j mod SETS == x; set 0 writes the output
+    const int x = SETS == 2 ? (warp - 4) >> 2 : 0;
     const int q = warp & 3;          // TMEM lane quarter
     const int r = q * 32 + lane;     // row inside the tile
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sl2 = a.scale_log2e;
-    // m: running row maximum of the scaled scores (log2 units), raised lazily; l: the row's sum of
-    // 2^(s - m) over the keys so far.
+    // m: running row maximum of the scaled scores (log2 units), raised lazily, as last decided (by
+    // either set); l: this set's part of the row's sum of 2^(s - m) over its keys so far.
     float m = -INFINITY, l = 0.f;
     bool ok = start_ok;
-    uint32_t pid = NB_P;   // NB_P + j mod kPIds
+    uint32_t pid = NB_P + x;   // NB_P + j mod kPIds for this set's tile j
+    float* m_row = reinterpret_cast<float*>(smem + OFF_MROW);
+    float* l_row = reinterpret_cast<float*>(smem + OFF_LROW);
+    // (two sets) take the maximum decided at tile jj by the other set; this set's sum follows a raise
+    auto msync = [&](int jj) {
+      named_sync(NB_M + (jj & 1), kNbM);
+      const float mp = m_row[r];
+      if (mp > m) {
+        l *= ex2_approx(m - mp);
+        m = mp;
+      }
+    };
     // One key tile.  The diagonal tile (DIAG) has its own instantiation, peeled out of the loop, so
     // that the loop body holds only the code of ordinary tiles.
     auto tile = [&](int j, auto diag_tag) {
       constexpr bool DIAG = decltype(diag_tag)::value;
       const int sb = j & 1;
-      // one pass of work; a failed wait leaves it early (break), the tile's barrier generation is
-      // still met below
+      // one pass of work; a failed wait leaves it early (break), the tile's barrier generations are
+      // still met below, in the same order
+      bool published = false;
       do {
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, ctl, W_SM_S));
       if (!ok) break;
@@ -550,9 +583,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           bm[bb] = fmax3(c0, c1, fmaxf(c2, c3));
         }
       }
+      if (SETS == 2 && j > 0) msync(j - 1);
       const float mt = fmax3(bm[0], bm[1], fmaxf(bm[2], bm[3])) * sl2;
       const bool need = mt > m + RESCALE_LOG2;   // true at j = 0
       const float m_new = need ? mt : m;
+      if constexpr (SETS == 2) {   // publish this tile's decision for the other set's next tile
+        m_row[r] = m_new;
+        __threadfence_block();
+        named_arrive(NB_M + (j & 1), kNbM);
+        published = true;
+      }
       if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
         // rescale this warp's O rows (factor 1 for rows that keep m) once the previous P.V, the
         // last writer of O, has completed: the scores of tile j + 1 are computed after it (the
@@ -615,17 +655,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       } while (false);
       // P of this tile is written (or this warp gave up: then it blocks, so that it can never
       // arrive on a later generation before the MMA warp has passed this one)
+      if (SETS == 2 && !published) {
+        if (j > 0) msync(j - 1);
+        named_arrive(NB_M + (j & 1), kNbM);
+      }
       if (ok) {
         tc_fence_before();
         named_arrive(pid, kNbP);
       } else {
         named_sync(pid, kNbP);
       }
-      pid = pid == NB_P + kPIds - 1 ? NB_P : pid + 1;
+      if constexpr (SETS == 2) pid = pid >= NB_P + 1 ? pid - 1 : pid + 2;   // tile j + 2
+      else pid = pid == NB_P + kPIds - 1 ? NB_P : pid + 1;
     };
-    for (int j = 0; j < t; ++j) tile(j, std::false_type{});
-    tile(t, std::true_type{});
-    // ---- epilogue: O / l -> BF16 (and/or MXFP8), LSE
+    for (int j = x; j < t; j += SETS) tile(j, std::false_type{});
+    if (SETS == 1 || (t & 1) == x) tile(t, std::true_type{});
+    else msync(t);   // the final maximum, decided by the other set
+    if constexpr (SETS == 2) {   // set 1's part of the row sum (relative to the final maximum) to set 0
+      if (x == 1) {
+        l_row[r] = l;
+        __threadfence_block();
+        named_arrive(NB_L, kNbM);
+      } else {
+        named_sync(NB_L, kNbM);
+        l += l_row[r];
+      }
+    }
+    // ---- epilogue (set 0): O / l -> BF16 (and/or MXFP8), LSE
+    if (x != 0) ok = false;
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(B_O_FULL), 0, ctl, W_SM_O));
     if (ok) {
       tc_fence_after();
@@ -704,7 +761,7 @@ cudaError_t launch_variant(const AttnArgs& args, cudaStream_t st) {
     __atomic_fetch_or(&set_mask, bit, __ATOMIC_ACQ_REL);
   }
   const long long ctas = (long long)args.B * args.Hq * ((args.S + BM - 1) / BM);
-  kern<<<(unsigned)ctas, kThreads, SMEM_BYTES, st>>>(args);
+  kern<<<(unsigned)ctas, kThreadsFor<P_TERMS>, SMEM_BYTES, st>>>(args);
   return cudaGetLastError();
 }
 

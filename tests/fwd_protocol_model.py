@@ -23,9 +23,14 @@ Semantics modelled:
 
 `n_pids` is the number of named-barrier IDs the P hand-over (softmax -> MMA warp) rotates through:
 3 as built; 2 (tile parity) is the earlier form, which the model shows can mix generations and
-deadlock once a wait gives up mid-run.  `mistake` plants a protocol error, so that the tests can show
-the model catches one: "no_stage_wait" (the producer refills a K/V stage without waiting for the
-scores that prove its last reader completed).
+deadlock once a wait gives up mid-run.  `sets` is the number of softmax sets: 1 (four warps take every
+key tile; the kernel with one P term) or 2 (two sets of four take alternate tiles and hand each other
+the running row maximum at the NB_M barriers, set 1 its row sum at NB_L; the kernel with two P terms).
+`mistake` plants a protocol error, so that the tests can show the model catches one: "no_stage_wait"
+(the producer refills a K/V stage without waiting for the scores that prove its last reader
+completed), "publish_before_take" (two sets: a set publishes its tile's maximum before taking the
+previous tile's), "no_final_take" (two sets: the set that does not own the last tile hands over its
+row sum without the final maximum).
 """
 import random
 
@@ -63,8 +68,8 @@ class _MBar:
 
 
 class _World:
-    def __init__(self, t, own, seed, rescale_p, abort_p, n_pids, mistake=None):
-        self.mistake = mistake
+    def __init__(self, t, own, seed, rescale_p, abort_p, n_pids, mistake=None, sets=1):
+        self.mistake, self.sets = mistake, sets
         self.rng = random.Random(seed)
         self.t, self.own, self.rescale_p, self.abort_p, self.n_pids = t, own, rescale_p, abort_p, n_pids
         self.aborted = False
@@ -300,14 +305,97 @@ def _softmax(w, q):
         w.read("O%d" % q, t + 1, "epilogue%d" % q)
 
 
-def run(t, own, seed, rescale_p=0.3, abort_p=0.0, n_pids=3, mistake=None, max_idle=200000):
+def _softmax_set(w, x, q):
+    """One softmax warp of set x (two sets): tiles j with j % 2 == x, rows of lane quarter q."""
+    t = w.t
+    ok = True
+    seen = [-1]   # the latest tile whose maximum this warp knows
+
+    def take(j):   # the maximum decided at tile j by the other set
+        yield from w.nb_sync("M%d" % (j & 1), 8, j)
+        if ok:
+            w.read("M%d" % q, j, "set%d softmax%d takes" % (x, q))
+        seen[0] = j
+
+    for j in range(x, t + 1, 2):
+        sb = j & 1
+        arrived = published = False
+        while True:   # one pass; break = gave up
+            if ok:
+                ok = yield from w.wait("S_FULL%d" % sb, (j >> 1) & 1)
+            if not ok:
+                break
+            w.read("S%d_%d" % (sb, q), ("S", j), "set%d softmax%d" % (x, q))
+            yield
+            if w.mistake == "publish_before_take":
+                w.write("M%d" % q, j, "set%d softmax%d publishes" % (x, q))
+                w.nb_arrive("M%d" % (j & 1), 8, j)
+                published = True
+                seen[0] = j
+            if j > 0:
+                yield from take(j - 1)
+            if not published:
+                w.write("M%d" % q, j, "set%d softmax%d publishes" % (x, q))
+                w.nb_arrive("M%d" % (j & 1), 8, j)
+                published = True
+                seen[0] = j
+            if j > 0 and w.rng.random() < w.rescale_p:
+                if j < t:
+                    ok = yield from w.wait("S_FULL%d" % ((j + 1) & 1), ((j + 1) >> 1) & 1)
+                else:
+                    ok = yield from w.wait("P_DONE", 0)
+                if not ok:
+                    break
+                w.read("O%d" % q, j, "rescale%d%d" % (x, q))
+                w.write("O%d" % q, j, "rescale%d%d" % (x, q))
+            w.write("S%d_%d" % (sb, q), ("P", j), "set%d softmax%d" % (x, q))
+            if w.own and j == t and t > 0:
+                ok = yield from w.wait("P_DONE", 0)
+                if not ok:
+                    break
+            if w.own and j == t:
+                w.write("S%d_%d" % ((t + 1) & 1, q), ("OWN", t), "set%d softmax%d" % (x, q))
+            w.write("SFP%d_%d" % (sb, q), ("P", j), "set%d softmax%d" % (x, q))
+            w.nb_arrive(w.pid(j), 5, j)
+            arrived = True
+            break
+        if not published:   # gave up first: meet the maximum generations in the same order
+            if j > 0:
+                yield from take(j - 1)
+            w.nb_arrive("M%d" % (j & 1), 8, j)
+            seen[0] = j
+        if not arrived:
+            yield from w.nb_sync(w.pid(j), 5, j)
+        yield
+    if (t & 1) != x and w.mistake != "no_final_take":
+        yield from take(t)
+    if not w.aborted and seen[0] != t:
+        raise ModelError("set%d softmax%d hands over its row sum without the final maximum" % (x, q))
+    if x == 1:
+        w.write("L%d" % q, 1, "set1 softmax%d" % q)
+        w.nb_arrive("L", 8, 0)
+    else:
+        yield from w.nb_sync("L", 8, 0)
+        if ok:
+            w.read("L%d" % q, 1, "set0 softmax%d" % q)
+        if ok:
+            ok = yield from w.wait("O_FULL", 0)
+        if ok:
+            w.read("O%d" % q, t + 1, "epilogue%d" % q)
+
+
+def run(t, own, seed, rescale_p=0.3, abort_p=0.0, n_pids=3, mistake=None, sets=1, max_idle=200000):
     """One interleaving; raises ModelError on a violation or a deadlock."""
-    w = _World(t, own, seed, rescale_p, abort_p, n_pids, mistake)
+    w = _World(t, own, seed, rescale_p, abort_p, n_pids, mistake, sets)
     roles = {"producer": _producer(w), "forwarder": _forwarder(w), "mma": _mma(w)}
     if own:
         roles["decoder"] = _decoder(w)
     for q in range(4):
-        roles["softmax%d" % q] = _softmax(w, q)
+        if sets == 1:
+            roles["softmax%d" % q] = _softmax(w, q)
+        else:
+            for x in range(2):
+                roles["set%d softmax%d" % (x, q)] = _softmax_set(w, x, q)
     idle = 0
     while roles or w.pipe or w.copies:
         choices = list(roles) + (["pipe"] if w.pipe else []) + ["copy%d" % i for i in range(len(w.copies))]
@@ -329,7 +417,7 @@ def run(t, own, seed, rescale_p=0.3, abort_p=0.0, n_pids=3, mistake=None, max_id
             raise ModelError("deadlock: %s still running" % ", ".join(sorted(roles)))
 
 
-def count_failures(seeds, tiles=(0, 1, 2, 3, 5, 8), abort_ps=(0.0, 0.002, 0.02), n_pids=3, mistake=None):
+def count_failures(seeds, tiles=(0, 1, 2, 3, 5, 8), abort_ps=(0.0, 0.002, 0.02), n_pids=3, mistake=None, sets=1):
     """Failures over seeds x tile counts x {own block, leaky} x abort rates; the first messages."""
     failures, first = 0, []
     for seed in range(seeds):
@@ -337,7 +425,7 @@ def count_failures(seeds, tiles=(0, 1, 2, 3, 5, 8), abort_ps=(0.0, 0.002, 0.02),
             for own in (True, False):
                 for ap in abort_ps:
                     try:
-                        run(t, own, seed * 1000 + t, abort_p=ap, n_pids=n_pids, mistake=mistake)
+                        run(t, own, seed * 1000 + t, abort_p=ap, n_pids=n_pids, mistake=mistake, sets=sets)
                     except ModelError as e:
                         failures += 1
                         if len(first) < 3:

@@ -28,6 +28,18 @@ def test_forward_two_p_ids_mix_generations_after_a_mid_run_abort():
     assert failures > 0
 
 
+def test_forward_two_softmax_sets_are_clean():
+    # the kernel with two P terms: two sets of softmax warps take alternate key tiles
+    failures, first = FM.count_failures(seeds=10, sets=2)
+    assert failures == 0, first
+
+
+@pytest.mark.parametrize("mistake", ["publish_before_take", "no_final_take"])
+def test_forward_two_set_model_catches_planted_mistakes(mistake):
+    failures, _ = FM.count_failures(seeds=6, tiles=(0, 1, 3, 6), abort_ps=(0.0,), sets=2, mistake=mistake)
+    assert failures > 0
+
+
 def test_forward_model_catches_a_missing_stage_wait():
     failures, _ = FM.count_failures(seeds=4, tiles=(5, 8), abort_ps=(0.0,), mistake="no_stage_wait")
     assert failures > 0
