@@ -93,17 +93,20 @@ def test_errors_launch_nothing(ops):
         ops.mxfp8_causal_attn_fwd(*args, layout=w.layout, p_terms=0, o=o, lse=lse)
 
 
-def test_bounded_wait_reports_timeout_and_context_survives(ops):
-    w = I.Workload("t", 1, 128, 1, 1)
+@pytest.mark.parametrize("S", [128, 640])
+@pytest.mark.parametrize("p_terms", [1, 2])   # one softmax set; two sets taking alternate key tiles
+def test_bounded_wait_reports_timeout_and_context_survives(ops, S, p_terms):
+    w = I.Workload("t", 1, S, 1, 1)
     args, _ = _quantised(ops, w)
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    ops.mxfp8_causal_attn_fwd(*args, layout=w.layout, softmax_scale=w.scale, dev_status=status,
+    ops.mxfp8_causal_attn_fwd(*args, layout=w.layout, softmax_scale=w.scale, p_terms=p_terms, dev_status=status,
                               wait_timeout_ms=200, debug_stall=1)
     assert ops.bsc_read_device_status(status) == ops.BSC_ERR_DEVICE_TIMEOUT
     assert int(status[0].item()) & 0x100
     # the context is still usable and a normal call gives a normal status
     status.zero_()
-    o, lse = ops.mxfp8_causal_attn_fwd(*args, layout=w.layout, softmax_scale=w.scale, dev_status=status)
+    o, lse = ops.mxfp8_causal_attn_fwd(*args, layout=w.layout, softmax_scale=w.scale, p_terms=p_terms,
+                                       dev_status=status)
     assert ops.bsc_read_device_status(status) == ops.BSC_OK
     assert torch.isfinite(o.float()).all()
 
