@@ -80,11 +80,12 @@ __device__ __forceinline__ uint2 decode4_bf16(uint32_t x, uint32_t scale2) {
 
 // ------------------------------------------------------------------------------------------------
 // prep.  Grid (Sp / 64, B * Hq, 4): block z picks the job, y the (batch, head) plane, x a run of
-// 64 rows; each of the 8 warps takes 8 rows.
-//   z = 0, 1, 2: Qh, Kh, Vt rows: 128 E4M3 bytes -> 128 BF16 (lane l takes bytes 4l..4l+3, whose
-//     scale is the row's block l / 8: Q and K rowwise scales, or V's one amplitude per token);
-//     planes past B * Hkv are idle for Kh and Vt;
-//   z = 3: statistics: Dlt_i = <dO_i, O_i> (fp32) and LSE_i log2(e).
+// 64 rows; each of the 8 warps takes 8 rows, with every load of its rows issued before any is used.
+//   z = 0, 1, 2: Qh, Kh, Vt rows: 128 E4M3 bytes -> 128 BF16; 8 lanes per row, lane l taking bytes
+//     16 l..16 l + 15, whose scale is the row's block l / 2 (Q and K rowwise scales) or V's one
+//     amplitude per token; a warp takes 4 rows per pass.  Planes past B * Hkv are idle for Kh and Vt;
+//   z = 3: statistics: Dlt_i = <dO_i, O_i> (fp32; lane l sums elements 4l..4l+3, then a butterfly
+//     over the warp) and LSE_i log2(e).
 // Rows at or past S: zero BF16 rows, Dlt = 0 and LSE = +inf, which make their P and dS exactly 0.
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ BwdArgs a) {
   const int lane = threadIdx.x & 31, job = blockIdx.z;
@@ -94,37 +95,64 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
   const int b = plane / H, h = plane - b * H;
   const int i0 = blockIdx.x * 64 + (threadIdx.x >> 5) * 8;
   const long long prow = (long long)plane * a.Sp;   // the plane's first row in the workspace
+  auto src_row = [&](int i) {
+    return a.layout == 0 ? ((long long)b * a.S + i) * H + h : ((long long)i * a.B + b) * H + h;
+  };
   if (job < 3) {
     const uint8_t* src = job == 0 ? a.q8 : job == 1 ? a.k8 : a.vtn;
     uint16_t* dst = job == 0 ? a.qh : job == 1 ? a.kh : a.vh;
-#pragma unroll 2
-    for (int i = i0; i < i0 + 8; ++i) {
-      uint2 out = make_uint2(0u, 0u);
+    const int r4 = lane >> 3, l8 = lane & 7;
+    uint4 x[2];
+    uint32_t sb[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = i0 + 4 * k + r4;
+      x[k] = make_uint4(0u, 0u, 0u, 0u);
+      sb[k] = 0u;
       if (i < a.S) {
-        const long long row = a.layout == 0 ? ((long long)b * a.S + i) * H + h : ((long long)i * a.B + b) * H + h;
-        const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(src + row * HD) + lane);
-        const uint32_t sb = job == 2 ? __ldg(a.vtn_sc + (long long)plane * a.S + i)
-                                     : __ldg((job == 0 ? a.q_sc : a.k_sc) + ((long long)plane * a.S + i) * 4 + (lane >> 3));
-        out = decode4_bf16(x, bf16x2_pow2_e8m0(sb));
+        x[k] = __ldg(reinterpret_cast<const uint4*>(src + src_row(i) * HD) + l8);
+        sb[k] = job == 2 ? __ldg(a.vtn_sc + (long long)plane * a.S + i)
+                         : __ldg((job == 0 ? a.q_sc : a.k_sc) + ((long long)plane * a.S + i) * 4 + (l8 >> 1));
       }
-      reinterpret_cast<uint2*>(dst + (prow + i) * HD)[lane] = out;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = i0 + 4 * k + r4;
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+      if (i < a.S) {
+        const uint32_t s2 = bf16x2_pow2_e8m0(sb[k]);
+        const uint2 d0 = decode4_bf16(x[k].x, s2), d1 = decode4_bf16(x[k].y, s2);
+        const uint2 d2 = decode4_bf16(x[k].z, s2), d3 = decode4_bf16(x[k].w, s2);
+        lo = make_uint4(d0.x, d0.y, d1.x, d1.y);
+        hi = make_uint4(d2.x, d2.y, d3.x, d3.y);
+      }
+      uint4* out = reinterpret_cast<uint4*>(dst + (prow + i) * HD) + 2 * l8;
+      out[0] = lo;
+      out[1] = hi;
     }
     return;
   }
   const long long plane_rows = (long long)a.B * a.Hq * a.Sp;
-#pragma unroll 2
-  for (int i = i0; i < i0 + 8; ++i) {
-    float acc = 0.f;
-    if (i < a.S) {
-      const long long row = a.layout == 0 ? ((long long)b * a.S + i) * a.Hq + h : ((long long)i * a.B + b) * a.Hq + h;
-      const uint2 x = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + row * HD) + lane);
-      const uint2 y = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + row * HD) + lane);
-      const uint32_t xs[2] = {x.x, x.y}, ys[2] = {y.x, y.y};
+  uint2 xo[8], yo[8];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
-        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
-      }
+  for (int k = 0; k < 8; ++k) {
+    const int i = i0 + k;
+    xo[k] = yo[k] = make_uint2(0u, 0u);
+    if (i < a.S) {
+      const long long row = src_row(i);
+      xo[k] = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + row * HD) + lane);
+      yo[k] = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + row * HD) + lane);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = i0 + k;
+    float acc = 0.f;
+    const uint32_t xs[2] = {xo[k].x, xo[k].y}, ys[2] = {yo[k].x, yo[k].y};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+      acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
