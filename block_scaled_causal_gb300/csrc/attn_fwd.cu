@@ -653,8 +653,9 @@ __global__ void __launch_bounds__(kThreadsFor<P_TERMS>, 1) attn_fwd_kernel(const
                    : "memory");
       tmem_st_wait();
       } while (false);
-      // P of this tile is written (or this warp gave up: then it blocks, so that it can never
-      // arrive on a later generation before the MMA warp has passed this one)
+      // P of this tile is written (or this warp gave up: then, with two sets, it still takes the
+      // previous tile's maximum and publishes one, in that order, and it blocks on the P generation,
+      // so that it can never arrive on a later generation before the MMA warp has passed this one)
       if (SETS == 2 && !published) {
         if (j > 0) msync(j - 1);
         named_arrive(NB_M + (j & 1), kNbM);
