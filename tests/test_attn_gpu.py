@@ -169,6 +169,19 @@ def test_full_size_sampled_rows(ops, name, p_terms):
         print(_compare(Og, Lg, O, L))
 
 
+@pytest.mark.parametrize("layout", [I.BSHD, I.SBHD])
+@pytest.mark.parametrize("p_terms", [1, 2])
+def test_large_partial_last_tile_sampled_rows(ops, layout, p_terms):
+    # S = 8K - 32: the last query and key tile holds 96 tokens; the sampled rows include the whole
+    # end of the sequence (the partial tile's rows and its last block)
+    w = dataclasses.replace(I.WORKLOADS["gqa_s8k_h16_kv4"], S=8192 - 32, layout=layout, B=1 if layout == I.BSHD else 2)
+    q, k, v = I.make_qkv(w)
+    Og, Lg = _run(ops, w, q, k, v, p_terms)
+    rows = _sample_rows(w.S)
+    O, L = _oracle(w, q, k, v, rows=rows)
+    print(_compare(Og[:, rows], Lg[:, :, rows], O, L))
+
+
 # ----------------------------------------------------------------------------------------------
 # Causality: perturbing every token after i leaves rows <= i bit-identical (O and LSE).
 
