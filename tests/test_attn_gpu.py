@@ -1,6 +1,7 @@
 """GPU leak-free causal MXFP8 attention forward against the fp64 oracle, through the C ABI.
 
-Tolerances: O within max-abs 3e-2 and mean-abs 3e-3 of the oracle and LSE within 1e-3 relative,
+Tolerances: O within max-abs 3e-2 and mean-abs 3e-3 of the oracle and LSE within 1e-3 relative
+(with an fp32 floor of 4e-6 for an LSE near 0),
 P's FP8 rounding being the only allowed difference.  O is returned in BF16, whose own rounding is
 half an ulp = 2^(floor(log2|O|) - 8): more than 3e-2 once |O| >= 8 (heavy-tailed V rows reach
 |O| ~ 20-60).  The max-abs check therefore allows 3e-2 plus half a BF16 ulp of the oracle value.
@@ -28,6 +29,10 @@ from tests._helpers import bshd_np
 pytestmark = pytest.mark.gpu
 
 MAX_ABS, MEAN_ABS, LSE_REL = 3e-2, 3e-3, 1e-3
+# LSE is fp32, formed as (m + log2 l) ln 2 from terms of magnitude below 32 at these shapes: one fp32
+# ulp of such a term (2^-18 = 3.8e-6) is the floor under the relative tolerance, which alone would ask
+# an LSE near 0 (a row whose few scores sum to about 1) for more than fp32 can hold.
+LSE_ABS = 4e-6
 
 
 @pytest.fixture(scope="module")
@@ -96,10 +101,11 @@ def bf16_half_ulp(x):
 
 def _compare(Og, Lg, O, L, bound=None):
     err = np.abs(Og - O)
-    lse_rel = np.abs(Lg - L) / np.maximum(np.abs(L), 1e-30)
-    info = "max %.3e mean %.3e lse_rel %.3e" % (err.max(), err.mean(), lse_rel.max())
+    lse_err = np.abs(Lg - L)
+    lse_rel = lse_err / np.maximum(np.abs(L), 1e-30)
+    info = "max %.3e mean %.3e lse_rel %.3e lse_abs %.3e" % (err.max(), err.mean(), lse_rel.max(), lse_err.max())
     assert np.all(np.isfinite(Og)), info
-    assert lse_rel.max() <= LSE_REL, info
+    assert np.all(lse_err <= LSE_REL * np.abs(L) + LSE_ABS), info
     if bound is None:
         excess = err - (MAX_ABS + bf16_half_ulp(O))
         assert excess.max() <= 0 and err.mean() <= MEAN_ABS, info + " excess over 3e-2 + half ulp %.3e" % excess.max()
