@@ -7,7 +7,10 @@ So each element must lie within
     dV: 2^-7 * sum_i P_ij |dO_i|            + half a BF16 ulp
     dK: 2^-7 * scale * sum_i |dS_ij| |Qh_i| + half a BF16 ulp
     dQ: 2^-7 * scale * sum_j |dS_ij| |Kh_j| + half a BF16 ulp
-of the oracle (twice the two roundings' bound, summed with absolute values).
+of the oracle (twice the two roundings' bound, summed with absolute values), where |dS| also carries
+the fp32 accumulation of dP = dO V^T and of Dlt = <dO, O> (each a sum of D = 128 products: at most
+128 * 2^-24 = 2^-17 of its absolute sum), which a cancelling dP - Dlt does not shrink:
+    |dS|_ij -> |dS_ij| + 2^-10 P_ij (|dO_i|.|V_j| + |dO_i|.|O_i|)     (2^-10 = 2^-17 / 2^-7).
 """
 import numpy as np
 import pytest
@@ -41,7 +44,8 @@ def _abs_terms(qh, kh, vt, o, lse, do, scale):
             s = scale * qh[b, :, hq] @ kh[b, :, hk].T
             p = np.where(mask, np.exp(np.where(mask, s, 0.0) - lse[b, hq][:, None]), 0.0)
             dp = do[b, :, hq] @ vt[b, :, hk].T
-            ds = np.abs(p * (dp - np.sum(do[b, :, hq] * o[b, :, hq], axis=1)[:, None]))
+            acc = np.abs(do[b, :, hq]) @ np.abs(vt[b, :, hk]).T + np.sum(np.abs(do[b, :, hq] * o[b, :, hq]), axis=1)[:, None]
+            ds = np.abs(p * (dp - np.sum(do[b, :, hq] * o[b, :, hq], axis=1)[:, None])) + 2.0 ** -10 * p * acc
             tv[b, :, hk] += p.T @ np.abs(do[b, :, hq])
             tk[b, :, hk] += scale * ds.T @ np.abs(qh[b, :, hq])
             tq[b, :, hq] += scale * ds @ np.abs(kh[b, :, hk])
@@ -112,7 +116,8 @@ def test_bwd_dq_causal_bit_exact(ops):
 
 
 def _abs_terms_sampled(qh, kh, vt, o, lse, do, scale, rows, keys):
-    """The tolerance terms of _abs_terms at the sampled dQ rows and dK, dV keys."""
+    """The tolerance terms of _abs_terms (with the same accumulation term in |dS|) at the sampled dQ rows
+    and dK, dV keys."""
     B, S, Hq, D = qh.shape
     g = Hq // kh.shape[2]
     tq = np.zeros((B, len(rows), Hq, D))
@@ -123,13 +128,16 @@ def _abs_terms_sampled(qh, kh, vt, o, lse, do, scale, rows, keys):
             hk = hq // g
             for n, i in enumerate(rows):
                 p = np.exp(scale * (kh[b, : i + 1, hk] @ qh[b, i, hq]) - lse[b, hq, i])
-                ds = np.abs(p * (vt[b, : i + 1, hk] @ do[b, i, hq] - np.dot(do[b, i, hq], o[b, i, hq])))
+                acc = np.abs(vt[b, : i + 1, hk]) @ np.abs(do[b, i, hq]) + np.sum(np.abs(do[b, i, hq] * o[b, i, hq]))
+                ds = np.abs(p * (vt[b, : i + 1, hk] @ do[b, i, hq] - np.dot(do[b, i, hq], o[b, i, hq]))) + 2.0 ** -10 * p * acc
                 tq[b, n, hq] = scale * ds @ np.abs(kh[b, : i + 1, hk])
             ri = np.arange(int(keys.min()), S)
             vis = keys[None, :] <= ri[:, None]
             p = np.where(vis, np.exp(np.where(vis, scale * qh[b, ri, hq] @ kh[b, keys, hk].T, 0.0)
                                      - lse[b, hq, ri][:, None]), 0.0)
-            ds = np.abs(p * (do[b, ri, hq] @ vt[b, keys, hk].T - np.sum(do[b, ri, hq] * o[b, ri, hq], axis=1)[:, None]))
+            acc = np.abs(do[b, ri, hq]) @ np.abs(vt[b, keys, hk]).T + np.sum(np.abs(do[b, ri, hq] * o[b, ri, hq]), axis=1)[:, None]
+            ds = np.abs(p * (do[b, ri, hq] @ vt[b, keys, hk].T - np.sum(do[b, ri, hq] * o[b, ri, hq], axis=1)[:, None])) \
+                + 2.0 ** -10 * p * acc
             tv[b, :, hk] += p.T @ np.abs(do[b, ri, hq])
             tk[b, :, hk] += scale * ds.T @ np.abs(qh[b, ri, hq])
     return tq, tk, tv

@@ -1,6 +1,7 @@
 """A seeded sweep of random small shapes, through the C ABI, against the oracle: the one-launch
-quantiser bit for bit (Q, K rowwise; V columnwise and token-normalised) and the attention forward
-within the tolerance (both P modes, so both softmax forms of the kernel), over batch sizes,
+quantiser bit for bit (Q, K rowwise; V columnwise and token-normalised), the attention forward
+within the tolerance (both P modes, so both softmax forms of the kernel) and, on six of the shapes,
+the backward within its bound, over batch sizes,
 sequence lengths that are any multiple of 32 (partial last tiles, single-block sequences), head
 ratios (MHA and GQA up to 8:1) and both layouts.  The shapes are drawn once from a fixed seed, so the
 sweep is the same on every run."""
@@ -61,3 +62,12 @@ def test_forward_within_tolerance(ops, B, S, Hq, Hkv, layout, p_terms):
     Og, Lg = T._run(ops, w, q, k, v, p_terms)
     O, L = T._oracle(w, q, k, v)
     print(T._compare(Og, Lg, O, L))
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,layout", SHAPES[:6])
+def test_backward_within_tolerance(ops, B, S, Hq, Hkv, layout):
+    # the backward's own per-element bound (tests/test_bwd_gpu.py): BF16 P and dS for the MMAs,
+    # fp32 accumulation, BF16 outputs
+    from tests import test_bwd_gpu as BW
+    w = I.Workload("r", B, S, Hq, Hkv, layout=layout)
+    print(BW._run_and_check(ops, w, S + 11 * Hq))
