@@ -1,7 +1,7 @@
 """A seeded sweep of random small shapes, through the C ABI, against the oracle: the one-launch
 quantiser bit for bit (Q, K rowwise; V columnwise and token-normalised), the attention forward
 within the tolerance (both P modes, so both softmax forms of the kernel) and, on six of the shapes,
-the backward within its bound, over batch sizes,
+the backward within its bound, and the causality invariant bit for bit, over batch sizes,
 sequence lengths that are any multiple of 32 (partial last tiles, single-block sequences), head
 ratios (MHA and GQA up to 8:1) and both layouts.  The shapes are drawn once from a fixed seed, so the
 sweep is the same on every run."""
@@ -71,3 +71,22 @@ def test_backward_within_tolerance(ops, B, S, Hq, Hkv, layout):
     from tests import test_bwd_gpu as BW
     w = I.Workload("r", B, S, Hq, Hkv, layout=layout)
     print(BW._run_and_check(ops, w, S + 11 * Hq))
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,layout", SHAPES[:6])
+@pytest.mark.parametrize("p_terms", [1, 2])
+def test_causality_bit_exact(ops, B, S, Hq, Hkv, layout, p_terms):
+    # every token after a random row i perturbed (q, k, v, and the V amax of i's own 32-block
+    # raised): rows <= i of O and LSE stay bit-identical, in either layout and P mode
+    w = I.Workload("r", B, S, Hq, Hkv, layout=layout)
+    q, k, v = I.make_qkv(w, seed_offset=S + 7 * Hq)
+    rng = np.random.default_rng(S * 31 + Hq)
+    o0, l0 = ops.forward(q.cuda(), k.cuda(), v.cuda(), layout, w.scale, p_terms=p_terms)
+    for i in sorted({int(rng.integers(0, S - 1)), S // 2 - 1, 32 * (S // 64)}):
+        qb, kb, vb = (I.to_bshd(t, layout) for t in (q, k, v))
+        q2, k2, v2 = (I.to_layout(t, layout).contiguous() for t in T._perturb_after(qb, kb, vb, i))
+        o1, l1 = ops.forward(q2.cuda(), k2.cuda(), v2.cuda(), layout, w.scale, p_terms=p_terms)
+        torch.cuda.synchronize()
+        a, b = I.to_bshd(o0, layout)[:, : i + 1], I.to_bshd(o1, layout)[:, : i + 1]
+        assert torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16)), i
+        assert torch.equal(l0[..., : i + 1].contiguous().view(torch.int32), l1[..., : i + 1].contiguous().view(torch.int32)), i
