@@ -1,7 +1,8 @@
 """A seeded sweep of random small shapes, through the C ABI, against the oracle: the one-launch
 quantiser bit for bit (Q, K rowwise; V columnwise and token-normalised), the attention forward
 within the tolerance (both P modes, so both softmax forms of the kernel) and, on six of the shapes,
-the backward within its bound, and the causality invariant bit for bit, over batch sizes,
+the backward within its bound, the causality invariant bit for bit, the MXFP8 O epilogue and the
+leaky control, over batch sizes,
 sequence lengths that are any multiple of 32 (partial last tiles, single-block sequences), head
 ratios (MHA and GQA up to 8:1) and both layouts.  The shapes are drawn once from a fixed seed, so the
 sweep is the same on every run."""
@@ -90,3 +91,19 @@ def test_causality_bit_exact(ops, B, S, Hq, Hkv, layout, p_terms):
         a, b = I.to_bshd(o0, layout)[:, : i + 1], I.to_bshd(o1, layout)[:, : i + 1]
         assert torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16)), i
         assert torch.equal(l0[..., : i + 1].contiguous().view(torch.int32), l1[..., : i + 1].contiguous().view(torch.int32)), i
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,layout", SHAPES[:6])
+def test_mxfp8_o_and_leaky_control(ops, B, S, Hq, Hkv, layout):
+    # the MXFP8 O epilogue (its value and rule checks, tests/test_o8_gpu.py) and the leaky control
+    # (own block on the columnwise V as well) against the leaky oracle
+    from oracle import attention as A
+    from tests import test_o8_gpu as O8
+    w = I.Workload("r", B, S, Hq, Hkv, layout=layout)
+    q, k, v = I.make_qkv(w, seed_offset=S + 7 * Hq)
+    o, o8, osc = O8._run(ops, w, q, k, v)
+    O8._check(w, o, o8, osc, O8._oracle(w, q, k, v)[0])
+    Og, Lg = T._run(ops, w, q, k, v, 2, leaky=1)
+    qh, kh, vc, _ = T._oracle_operands(w, q, k, v, None)
+    O, L = A.causal_attention(qh, kh, vc, vc, w.scale)
+    print(T._compare(Og, Lg, O, L))
