@@ -617,7 +617,7 @@ def main():
         "attn_ms": attn_avg,
         "mxfp8_o": {"ms_per_step": ms8, "attn_ms": attn8, "value": whole_job_tflops(flops, world, ms8)},
         "configs": configs or None,
-        "within_north_star_tolerance": ({"p_terms1": within[1], "p_terms2": within[2],
+        "within_o_tolerance": ({"p_terms1": within[1], "p_terms2": within[2],
                                          "headline_p_terms": args.p_terms} if configs else None),
         "wall_s_timed_region": t_wall,
     }
